@@ -1,0 +1,362 @@
+// Host side of the C ABI: argument validation, workspace carving, TMA
+// descriptor encoding and kernel launches.  Every entry point only enqueues
+// work on the caller's stream; nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "attn_bwd.h"
+#include "internal.h"
+
+namespace attnbwd {
+
+namespace {
+
+__device__ unsigned int g_error_word_storage = 0u;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+attn_status validate(const attn_bwd_params* p) {
+  if (!p) return ATTN_ERR_INVALID;
+  if (p->batch < 1 || p->num_heads < 1 || p->num_kv_heads < 1 || p->seq_q < 1 || p->seq_k < 1)
+    return ATTN_ERR_INVALID;
+  if (p->num_heads % p->num_kv_heads != 0) return ATTN_ERR_INVALID;
+  if (p->head_dim != 64 && p->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->dtype != ATTN_F32 && p->dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (p->layout != ATTN_LAYOUT_BHSD && p->layout != ATTN_LAYOUT_BSHD) return ATTN_ERR_INVALID;
+  if (!(p->dropout_prob >= 0.f && p->dropout_prob < 1.f)) return ATTN_ERR_INVALID;
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID;
+  if (p->causal != 0 && p->causal != 1) return ATTN_ERR_INVALID;
+  if (p->causal_offset < 0 || p->window < 0) return ATTN_ERR_INVALID;
+  if (p->has_mask != 0 && p->has_mask != 1) return ATTN_ERR_INVALID;
+  // row and element counts must fit the kernels' index arithmetic
+  const long long rows_q = (long long)p->batch * p->num_heads * p->seq_q;
+  const long long rows_k = (long long)p->batch * p->num_kv_heads * p->seq_k;
+  if (rows_q * p->head_dim >= (1LL << 40) || rows_k * p->head_dim >= (1LL << 40))
+    return ATTN_ERR_INVALID;
+  if ((long long)p->seq_q + p->causal_offset >= (1LL << 31)) return ATTN_ERR_INVALID;
+  if ((long long)p->batch * p->num_heads >= (1LL << 31) / 1024) return ATTN_ERR_INVALID;
+  const long long kv_tiles = (p->seq_k + 63) / 64;  // smallest key tile
+  if (kv_tiles * p->batch * p->num_kv_heads >= (1LL << 31)) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+// Workspace carve-up (each region 256-byte aligned):
+//   delta, lse2   [B*H][sq_pad] fp32
+//   dq_acc        fp32 dQ accumulator (bf16 only; fp32 accumulates in dQ)
+//   qt, dot, kt   transposed fp32 copies [B*H][D][sq_pad], [B*Hkv][D][sk_pad]
+//                 (fp32 only: TF32 products take K-major operands)
+struct WsLayout {
+  size_t delta, lse2, dq_acc, qt, dot, kt, total;
+  int sq_pad, sk_pad;
+};
+
+WsLayout ws_layout(const attn_bwd_params& p) {
+  WsLayout w;
+  w.sq_pad = round_up(p.seq_q, kRowPad);
+  w.sk_pad = round_up(p.seq_k, kRowPad);
+  const size_t rows = (size_t)p.batch * p.num_heads * w.sq_pad;
+  const bool bf = p.dtype == ATTN_BF16;
+  w.delta = 0;
+  w.lse2 = align256(rows * 4);
+  w.dq_acc = w.lse2 + align256(rows * 4);
+  const size_t dq = bf ? align256((size_t)p.batch * p.num_heads * p.seq_q * p.head_dim * 4) : 0;
+  w.qt = w.dq_acc + dq;
+  const size_t qt = bf ? 0 : align256(rows * p.head_dim * 4);
+  w.dot = w.qt + qt;
+  w.kt = w.dot + qt;
+  const size_t kt =
+      bf ? 0 : align256((size_t)p.batch * p.num_kv_heads * w.sk_pad * p.head_dim * 4);
+  w.total = w.kt + kt;
+  return w;
+}
+
+// Transposed fp32 copy [BH][D][s_pad]; the map's extent along s is the true
+// length, so TMA fills the padding columns with zeros.
+CUresult make_map_t(CUtensorMap* m, const void* base, int D, int S, int s_pad, int BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint64_t dims[4] = {(cuuint64_t)S, (cuuint64_t)D, (cuuint64_t)BH, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)s_pad * 4, (cuuint64_t)s_pad * D * 4,
+                           (cuuint64_t)s_pad * D * 4 * BH};
+  cuuint32_t box[4] = {32, (cuuint32_t)D, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_TFLOAT32, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int H, int B,
+                  int layout, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
+  const int e = dtype == ATTN_BF16 ? 2 : 4;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3];
+  if (layout == ATTN_LAYOUT_BHSD) {
+    strides[0] = (cuuint64_t)D * e;
+    strides[1] = (cuuint64_t)S * D * e;
+    strides[2] = (cuuint64_t)H * S * D * e;
+  } else {
+    strides[0] = (cuuint64_t)H * D * e;
+    strides[1] = (cuuint64_t)D * e;
+    strides[2] = (cuuint64_t)S * H * D * e;
+  }
+  cuuint32_t box[4] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  // fp32 tensors are fetched as TF32 (the operand type of the products)
+  return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_TFLOAT32,
+             4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+unsigned int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word_storage) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = reinterpret_cast<unsigned int*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+}  // namespace attnbwd
+
+using namespace attnbwd;
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+  }
+  return "unknown status";
+}
+
+size_t attn_bwd_workspace_size(const attn_bwd_params* p) {
+  if (validate(p) != ATTN_OK) return 0;
+  return ws_layout(*p).total;
+}
+
+attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                     const void* O, const void* dO, const float* LSE, const float* mask,
+                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                     void* stream_v) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return ATTN_ERR_INVALID;
+  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
+  const WsLayout wl = ws_layout(*p);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < wl.total)
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  float* delta = reinterpret_cast<float*>(ws + wl.delta);
+  float* lse2 = reinterpret_cast<float*>(ws + wl.lse2);
+  float* dq_acc = p->dtype == ATTN_BF16 ? reinterpret_cast<float*>(ws + wl.dq_acc)
+                                        : reinterpret_cast<float*>(dQ);
+
+  TileMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const int bm = dkdv_block_m(p->dtype, p->head_dim);
+  const int bn = dkdv_block_n(p->dtype, p->head_dim);
+  const bool fp32 = p->dtype != ATTN_BF16;
+  float* qt = reinterpret_cast<float*>(ws + wl.qt);
+  float* dot = reinterpret_cast<float*>(ws + wl.dot);
+  float* kt = reinterpret_cast<float*>(ws + wl.kt);
+  if (fp32 && (make_map_t(&maps.qt, qt, p->head_dim, p->seq_q, wl.sq_pad,
+                          p->batch * p->num_heads) != CUDA_SUCCESS ||
+               make_map_t(&maps.dot, dot, p->head_dim, p->seq_q, wl.sq_pad,
+                          p->batch * p->num_heads) != CUDA_SUCCESS ||
+               make_map_t(&maps.kt, kt, p->head_dim, p->seq_k, wl.sk_pad,
+                          p->batch * p->num_kv_heads) != CUDA_SUCCESS))
+    return ATTN_ERR_CUDA;
+  if (make_map(&maps.q, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
+               bm) != CUDA_SUCCESS ||
+      make_map(&maps.dout, dO, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch,
+               p->layout, bm) != CUDA_SUCCESS ||
+      make_map(&maps.k, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
+               bn) != CUDA_SUCCESS ||
+      make_map(&maps.v, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
+               bn) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+
+  TileArgs a;
+  memset(&a, 0, sizeof(a));
+  a.B = p->batch;
+  a.H = p->num_heads;
+  a.Hkv = p->num_kv_heads;
+  a.Sq = p->seq_q;
+  a.Sk = p->seq_k;
+  a.D = p->head_dim;
+  a.group = p->num_heads / p->num_kv_heads;
+  a.sq_pad = wl.sq_pad;
+  a.layout = p->layout;
+  a.scale = p->scale;
+  a.scale_log2e = p->scale * kLog2e;
+  a.causal = p->causal;
+  a.causal_offset = p->causal_offset;
+  a.window = p->window;
+  a.has_mask = p->has_mask;
+  a.msb = p->mask_stride_b;
+  a.msh = p->mask_stride_h;
+  a.msq = p->mask_stride_q;
+  a.msk = p->mask_stride_k;
+  a.mask = mask;
+  a.dropout = p->dropout_prob > 0.f ? 1 : 0;
+  a.drop_threshold = dropout_threshold(p->dropout_prob);
+  a.drop_inv_keep = (float)(1.0 / (1.0 - (double)p->dropout_prob));
+  a.seed_lo = (uint32_t)(p->seed & 0xFFFFFFFFu);
+  a.seed_hi = (uint32_t)(p->seed >> 32);
+  a.lse2 = lse2;
+  a.delta = delta;
+  a.dq_acc = dq_acc;
+  a.dK = dK;
+  a.dV = dV;
+  a.n_kv_tiles = (p->seq_k + bn - 1) / bn;
+  a.err = err;
+
+  if (launch_prep(*p, O, dO, LSE, delta, lse2, wl.sq_pad, dq_acc, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (fp32 && (launch_transpose(static_cast<const float*>(Q), qt, p->batch, p->num_heads,
+                                p->seq_q, p->head_dim, wl.sq_pad, p->layout, stream) != cudaSuccess ||
+               launch_transpose(static_cast<const float*>(dO), dot, p->batch, p->num_heads,
+                                p->seq_q, p->head_dim, wl.sq_pad, p->layout, stream) != cudaSuccess ||
+               launch_transpose(static_cast<const float*>(K), kt, p->batch, p->num_kv_heads,
+                                p->seq_k, p->head_dim, wl.sk_pad, p->layout, stream) != cudaSuccess))
+    return ATTN_ERR_CUDA;
+  if (launch_dkdv(*p, maps, a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (p->dtype == ATTN_BF16 && launch_dq_convert(*p, dq_acc, dQ, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+static attn_status validate_decode(const attn_bwd_decode_params* p) {
+  if (!p) return ATTN_ERR_INVALID;
+  if (p->num_seqs < 1 || p->n_heads < 1 || p->n_kv_heads < 1 || p->history_len < 1)
+    return ATTN_ERR_INVALID;
+  if (p->n_heads % p->n_kv_heads != 0) return ATTN_ERR_INVALID;
+  const int G = p->n_heads / p->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)p->num_seqs * p->n_heads >= 65536LL * 65535LL) return ATTN_ERR_INVALID;
+  if ((long long)p->num_seqs * p->n_kv_heads > 65535 || p->n_heads > 65535 ||
+      p->num_seqs > 65535)
+    return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+size_t attn_bwd_decode_workspace_size(const attn_bwd_decode_params* p) {
+  if (validate_decode(p) != ATTN_OK) return 0;
+  return align256(decode_partials_floats(*p, decode_num_splits(*p)) * 4);
+}
+
+attn_status attn_bwd_decode(const attn_bwd_decode_params* p, const float* k_hist,
+                            const float* v_hist, const float* probs, const float* d_out,
+                            float* d_scores, float* d_q, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  attn_status st = validate_decode(p);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[] = {k_hist, v_hist, probs, d_out, d_scores, d_q};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return ATTN_ERR_INVALID;
+  const int n_split = decode_num_splits(*p);
+  const size_t need = align256(decode_partials_floats(*p, n_split) * 4);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  if (launch_decode(*p, k_hist, v_hist, probs, d_out, d_scores, d_q,
+                    reinterpret_cast<float*>(workspace), n_split,
+                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_dropout_keep_mask(const attn_bwd_params* p, int32_t b, int32_t h, uint8_t* keep,
+                                   void* stream) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!keep || b < 0 || b >= p->batch || h < 0 || h >= p->num_heads) return ATTN_ERR_INVALID;
+  if (launch_dropout_mask(*p, b, h, keep, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_query_range(const attn_bwd_params* p, int32_t k0, int32_t k1,
+                                 int32_t* q_begin, int32_t* q_end) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!q_begin || !q_end || k0 < 0 || k1 < k0 || k1 >= p->seq_k) return ATTN_ERR_INVALID;
+  int b = 0, e = 0;
+  query_range(p->seq_q, p->causal, p->causal_offset, p->window, k0, k1, &b, &e);
+  *q_begin = b;
+  *q_end = e;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_check_device_error(int32_t clear_it) {
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear_it && v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return v == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+attn_status attn_selftest_mma(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t a_mn,
+                              int32_t b_mn, const void* A, const void* B, float* C,
+                              float* tmem_dump, void* stream) {
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  return selftest_mma_launch(dtype, M, N, K, a_mn, b_mn, A, B, C, tmem_dump,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,641 @@
+// Fused attention backward tile kernel for sm_103a (tcgen05 + TMA + TMEM).
+//
+// One CTA owns a tile of BN keys of one (batch, KV head) and walks the query
+// tiles of every query head that shares that KV head (the GQA group loop of
+// the WGSL page's flash_bwd_dk_dv), so dK and dV accumulate in tensor memory
+// without atomics.  Per query tile of BM rows it issues the five dense
+// products of the backward pass on the tensor cores:
+//   GEMM1  S^T  [BN,BM] = K . Q^T              (scores, unscaled)
+//   GEMM2  dP^T [BN,BM] = V . dO^T
+//   GEMM3  dV   [BN,D] += (P o M)^T . dO
+//   GEMM4  dK   [BN,D] += dS'^T . Q            (dS' = scale * dS)
+//   GEMM5  dQ^T [D,BM]  = K^T . dS'^T          (or dQ [BM,D] = dS' . K)
+// and adds dQ into an fp32 accumulator with global atomics (instead of the
+// WGSL page's separate atomic-free dQ pass, which would recompute GEMM1/2).
+//
+// Operand staging.  Shared-memory tiles are 128-byte swizzled row tiles,
+// [column block][row][128 bytes] with the 16-byte chunk index XOR (row & 7):
+// exactly what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B.
+//  * bf16: one copy of each tile serves as a K-major operand (rows = M/N) and
+//    as an MN-major operand (rows = K).
+//  * fp32 (TF32 products): the tensor cores take TF32 operands K-major only,
+//    so the contractions over queries (GEMM3/4) and keys (GEMM5) read
+//    transposed copies Q^T, dO^T, K^T that the transpose pre-pass writes to
+//    the workspace, and the softmax group also writes dS' in [query][key]
+//    orientation.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: K/V (and K^T) once, then per query tile Q, dO
+//               (and Q^T, dO^T), LSE2 and Delta into a ring of ST stages
+//   warp 1      MMA issuer (one elected lane)
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax group: one key row per TMEM lane; turns S^T and dP^T
+//               into P o M and dS' and stores them to shared memory as MMA
+//               operands; at the end writes dK and dV
+//   warps 8-11  dQ group: drains the GEMM5 accumulator into global memory
+// Accumulators with M = 64 rows live in lanes 0-15 of each 32-lane TMEM
+// sub-partition (row r -> lane (r / 16) * 32 + r % 16); M = 128 rows map
+// one-to-one.  Every tcgen05.ld is executed by whole warps.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "philox.cuh"
+#include "ptx.cuh"
+
+namespace attnbwd {
+
+namespace {
+
+template <bool BF16, int D>
+struct Cfg;
+template <>
+struct Cfg<false, 64> {  // fp32, D = 64
+  static constexpr int BN = 128, BM = 32, ST = 2;
+  static constexpr bool KMAJ = true, DQT = true;
+};
+template <>
+struct Cfg<false, 128> {  // fp32, D = 128
+  static constexpr int BN = 64, BM = 32, ST = 1;
+  static constexpr bool KMAJ = true, DQT = true;
+};
+template <>
+struct Cfg<true, 64> {  // bf16, D = 64
+  static constexpr int BN = 128, BM = 128, ST = 2;
+  static constexpr bool KMAJ = false, DQT = false;
+};
+template <>
+struct Cfg<true, 128> {  // bf16, D = 128
+  static constexpr int BN = 128, BM = 64, ST = 3;
+  static constexpr bool KMAJ = false, DQT = true;
+};
+
+template <bool BF16, int D>
+struct Layout {
+  using C = Cfg<BF16, D>;
+  static constexpr int BM = C::BM, ST = C::ST, BN = C::BN;
+  static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT;
+  static constexpr int E = BF16 ? 2 : 4;  // element bytes
+  static constexpr int W = 128 / E;       // elements per 128-byte segment
+  static constexpr int KSTEP = 32 / E;    // K elements per MMA instruction
+  static constexpr int NB_D = D / W;      // column blocks of a D-wide row tile
+  static constexpr int K_BYTES = BN * D * E;
+  static constexpr int Q_BYTES = BM * D * E;
+  static constexpr int P_BYTES = BN * BM * E;
+  // shared memory map (offsets from a 1024-aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + K_BYTES;  // must follow K (padded GEMM5 reads it)
+  static constexpr int OFF_KT = OFF_V + K_BYTES;
+  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);
+  static constexpr int OFF_DO = OFF_Q + ST * Q_BYTES;
+  static constexpr int OFF_QT = OFF_DO + ST * Q_BYTES;
+  static constexpr int OFF_DOT = OFF_QT + (KMAJ ? ST * Q_BYTES : 0);
+  static constexpr int OFF_P = OFF_DOT + (KMAJ ? ST * Q_BYTES : 0);
+  static constexpr int OFF_DS = OFF_P + P_BYTES;
+  static constexpr int OFF_DSN = OFF_DS + P_BYTES;
+  static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? P_BYTES : 0);
+  static constexpr int OFF_DELTA = OFF_LSE + ST * BM * 4;
+  static constexpr int OFF_BAR = OFF_DELTA + ST * BM * 4;
+  static constexpr int NUM_BARS = 2 * ST + 7;
+  static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
+  // bytes landing per stage and for the resident key tiles
+  static constexpr int STAGE_TX = (KMAJ ? 4 : 2) * Q_BYTES + 2 * BM * 4;
+  static constexpr int KV_TX = (KMAJ ? 3 : 2) * K_BYTES;
+  // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
+  static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
+  static constexpr int N5 = DQT ? BM : D;
+  // tensor memory columns
+  static constexpr int T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + D,
+                       T_DQ = 2 * BM + 2 * D;
+  static constexpr int T_USED = T_DQ + N5;
+  static constexpr int T_ALLOC = T_USED <= 256 ? 256 : 512;
+  static_assert(T_USED <= 512, "tensor memory budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BM % 32 == 0 && (BM % W == 0 || BM < W), "query tile");
+  static_assert(!KMAJ || BM % W == 0, "transposed tiles are whole 128-byte blocks");
+  static_assert(BN == 64 || BN == 128, "key tile");
+  static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
+};
+
+constexpr int kThreads = 384;
+
+__device__ __forceinline__ uint32_t sw_off(int blk, int rows, int row, int pos_bytes) {
+  return (uint32_t)(blk * rows * 128 + row * 128 + ((((pos_bytes >> 4) ^ (row & 7))) << 4) +
+                    (pos_bytes & 15));
+}
+
+// Accumulator row held by TMEM lane `lane128` (0..127) for an M-row product;
+// -1 for lanes that hold no row (M = 64 uses 16 lanes per sub-partition).
+template <int M>
+__device__ __forceinline__ int acc_row(int lane128) {
+  if constexpr (M == 128) {
+    return lane128;
+  } else {
+    return (lane128 & 31) < 16 ? (lane128 >> 5) * 16 + (lane128 & 15) : -1;
+  }
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Bounded wait that ignores the error word: used only on the unwinding path to
+// let copies or products already in flight land before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles / 4) return;
+  }
+}
+
+struct TileWork {
+  int b, kvh, k0, q_begin, q_end, q_first, tiles_per_head, total;
+};
+
+template <int BN, int BM>
+__device__ __forceinline__ TileWork tile_work(const TileArgs& a) {
+  TileWork w;
+  const int bh = blockIdx.x % (a.B * a.Hkv);
+  const int kt = blockIdx.x / (a.B * a.Hkv);
+  w.b = bh / a.Hkv;
+  w.kvh = bh % a.Hkv;
+  w.k0 = kt * BN;
+  const long long k1 = (long long)min(w.k0 + BN, a.Sk) - 1;
+  query_range(a.Sq, a.causal, a.causal_offset, a.window, w.k0, k1, &w.q_begin, &w.q_end);
+  w.q_first = (w.q_begin / BM) * BM;
+  w.tiles_per_head = w.q_end > w.q_begin ? (w.q_end - w.q_first + BM - 1) / BM : 0;
+  w.total = w.tiles_per_head * a.group;
+  return w;
+}
+
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_qt,
+                const __grid_constant__ CUtensorMap tm_kt,
+                const __grid_constant__ CUtensorMap tm_dot, const TileArgs a) {
+  using L = Layout<BF16, D>;
+  constexpr int BM = L::BM, ST = L::ST, BN = L::BN, W = L::W, E = L::E;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* full = bars;              // [ST] stage loaded (TMA tx)
+  uint64_t* empty = bars + ST;        // [ST] stage consumed (MMA commit)
+  uint64_t* kv_full = bars + 2 * ST;  // resident key tiles loaded
+  uint64_t* s_full = kv_full + 1;     // GEMM1/2 done
+  uint64_t* p_full = kv_full + 2;     // P / dS' in smem (128 arrivals)
+  uint64_t* mma5_done = kv_full + 3;  // GEMM3/4/5 done
+  uint64_t* dq_free = kv_full + 4;    // dQ accumulator drained (128 arrivals)
+  uint64_t* acc_done = kv_full + 5;   // all products done
+  uint64_t* final_bar = kv_full + 6;  // unwinding: products in flight done
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const TileWork w = tile_work<BN, BM>(a);
+  const int T = w.total;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(kv_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(mma5_done, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(final_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_ptr, L::T_ALLOC);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_sync() && T > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const int bhkv = w.b * a.Hkv + w.kvh;
+      mbar_expect_tx(kv_full, L::KV_TX);
+      for (int cb = 0; cb < L::NB_D; ++cb) {
+        tma_load_4d(smem + L::OFF_K + cb * BN * 128, &tm_k, kv_full, cb * W, w.k0, w.kvh, w.b);
+        tma_load_4d(smem + L::OFF_V + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh, w.b);
+      }
+      if constexpr (L::KMAJ) {
+        // K^T [D rows][BN keys]: one box of W keys x D rows per column block
+        for (int cb = 0; cb < BN / W; ++cb)
+          tma_load_4d(smem + L::OFF_KT + cb * D * 128, &tm_kt, kv_full, w.k0 + cb * W, 0, bhkv,
+                      0);
+      }
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % ST;
+        if (t >= ST && !mbar_wait(&empty[s], ((t / ST) - 1) & 1, a.err)) break;
+        const int g = t / w.tiles_per_head;
+        const int h = w.kvh * a.group + g;
+        const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
+        mbar_expect_tx(&full[s], L::STAGE_TX);
+        for (int cb = 0; cb < L::NB_D; ++cb) {
+          tma_load_4d(smem + L::OFF_Q + s * L::Q_BYTES + cb * BM * 128, &tm_q, &full[s], cb * W,
+                      q0, h, w.b);
+          tma_load_4d(smem + L::OFF_DO + s * L::Q_BYTES + cb * BM * 128, &tm_do, &full[s],
+                      cb * W, q0, h, w.b);
+        }
+        if constexpr (L::KMAJ) {
+          const int bh = w.b * a.H + h;
+          for (int cb = 0; cb < BM / W; ++cb) {
+            tma_load_4d(smem + L::OFF_QT + s * L::Q_BYTES + cb * D * 128, &tm_qt, &full[s],
+                        q0 + cb * W, 0, bh, 0);
+            tma_load_4d(smem + L::OFF_DOT + s * L::Q_BYTES + cb * D * 128, &tm_dot, &full[s],
+                        q0 + cb * W, 0, bh, 0);
+          }
+        }
+        const long long row = (long long)(w.b * a.H + h) * a.sq_pad + q0;
+        bulk_load(smem + L::OFF_LSE + s * BM * 4, a.lse2 + row, BM * 4, &full[s]);
+        bulk_load(smem + L::OFF_DELTA + s * BM * 4, a.delta + row, BM * 4, &full[s]);
+        issued = t + 1;
+      }
+      // let every copy still in flight land before the CTA can exit
+      drain_wait(kv_full, 0);
+      for (int t = (issued > ST ? issued - ST : 0); t < issued; ++t)
+        drain_wait(&full[t % ST], (t / ST) & 1);
+    }
+    __syncwarp();  // reconverge before the block-wide barrier at the end
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_sync() && T > 0) {
+      const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
+      const uint32_t sKT = smem_u32(smem + L::OFF_KT);
+      const uint32_t sP = smem_u32(smem + L::OFF_P), sdS = smem_u32(smem + L::OFF_DS);
+      const uint32_t sdSN = smem_u32(smem + L::OFF_DSN);
+      constexpr uint32_t id_s = make_idesc(BF16, BN, BM, false, false);
+      constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, !L::KMAJ);
+      constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, !L::KMAJ, !L::KMAJ);
+      bool ok = mbar_wait(kv_full, 0, a.err);
+      auto issue_front = [&](int t) {  // GEMM1, GEMM2 of tile t
+        const int s = t % ST;
+        const uint32_t sQ = smem_u32(smem + L::OFF_Q + s * L::Q_BYTES);
+        const uint32_t sDO = smem_u32(smem + L::OFF_DO + s * L::Q_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < D / L::KSTEP; ++ks) {
+          const int kb = ks * 32;
+          const uint32_t ka = (kb / 128) * BN * 128 + (kb % 128);
+          const uint32_t qa = (kb / 128) * BM * 128 + (kb % 128);
+          mma_ss<BF16>(tmem + L::T_S, sw128_desc(sK + ka, 16, 1024), sw128_desc(sQ + qa, 16, 1024),
+                       id_s, ks > 0);
+          mma_ss<BF16>(tmem + L::T_DP, sw128_desc(sV + ka, 16, 1024),
+                       sw128_desc(sDO + qa, 16, 1024), id_s, ks > 0);
+        }
+        mma_commit(s_full);
+      };
+      auto issue_back = [&](int t) -> bool {  // GEMM3, GEMM4, GEMM5 of tile t
+        const int s = t % ST;
+#pragma unroll
+        for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
+          const int kb = ks * 32;
+          const uint32_t pa = (kb / 128) * BN * 128 + (kb % 128);
+          const uint32_t acc = (t > 0 || ks > 0) ? 1u : 0u;
+          uint64_t bdo, bq;
+          if constexpr (L::KMAJ) {  // transposed tiles [D rows][BM], K-major
+            const uint32_t ta = (kb / 128) * D * 128 + (kb % 128);
+            bdo = sw128_desc(smem_u32(smem + L::OFF_DOT + s * L::Q_BYTES) + ta, 16, 1024);
+            bq = sw128_desc(smem_u32(smem + L::OFF_QT + s * L::Q_BYTES) + ta, 16, 1024);
+          } else {  // natural tiles [BM rows][D] read MN-major
+            const uint32_t ra = ks * L::KSTEP * 128;
+            bdo = sw128_desc(smem_u32(smem + L::OFF_DO + s * L::Q_BYTES) + ra, BM * 128, 1024);
+            bq = sw128_desc(smem_u32(smem + L::OFF_Q + s * L::Q_BYTES) + ra, BM * 128, 1024);
+          }
+          mma_ss<BF16>(tmem + L::T_DV, sw128_desc(sP + pa, 16, 1024), bdo, id_acc, acc);
+          mma_ss<BF16>(tmem + L::T_DK, sw128_desc(sdS + pa, 16, 1024), bq, id_acc, acc);
+        }
+        if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
+          if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T, both K-major over keys
+            const int kb = ks * 32;
+            const uint32_t ka = (kb / 128) * D * 128 + (kb % 128);
+            const uint32_t na = (kb / 128) * BM * 128 + (kb % 128);
+            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sKT + ka, 16, 1024),
+                         sw128_desc(sdSN + na, 16, 1024), id_dq, ks > 0);
+          } else if constexpr (L::DQT) {
+            const uint32_t ra = ks * L::KSTEP * 128;
+            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sK + ra, BN * 128, 1024),
+                         sw128_desc(sdS + ra, BN * 128, 1024), id_dq, ks > 0);
+          } else {
+            const uint32_t ra = ks * L::KSTEP * 128;
+            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sdS + ra, BN * 128, 1024),
+                         sw128_desc(sK + ra, BN * 128, 1024), id_dq, ks > 0);
+          }
+        }
+        mma_commit(mma5_done);
+        mma_commit(&empty[s]);
+        return true;
+      };
+      // With two or more stages GEMM1/2 of tile t are issued before GEMM3-5 of
+      // tile t-1, so the softmax group can start on tile t while the tensor
+      // cores finish t-1.  With one stage tile t's operands only arrive after
+      // GEMM3-5 of t-1 released the stage, so the order is back(t-1), front(t).
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % ST;
+        if (ST == 1 && t > 0) {
+          if (!mbar_wait(p_full, (t - 1) & 1, a.err)) { ok = false; break; }
+          tc_fence_after();
+          if (!issue_back(t - 1)) { ok = false; break; }
+        }
+        if (!mbar_wait(&full[s], (t / ST) & 1, a.err)) { ok = false; break; }
+        if (ST > 1 && t > 0 && !mbar_wait(p_full, (t - 1) & 1, a.err)) { ok = false; break; }
+        tc_fence_after();
+        issue_front(t);
+        if (ST > 1 && t > 0 && !issue_back(t - 1)) { ok = false; break; }
+      }
+      if (ok) {
+        if (mbar_wait(p_full, (T - 1) & 1, a.err)) {
+          tc_fence_after();
+          if (issue_back(T - 1)) mma_commit(acc_done);
+        }
+      }
+      mma_commit(final_bar);
+    }
+    __syncwarp();  // reconverge before the block-wide barrier at the end
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ softmax group
+    const int j = acc_row<BN>((warp - 4) * 32 + lane);  // key row of this lane, or -1
+    const int kj = w.k0 + (j >= 0 ? j : 0);
+    const bool key_ok = j >= 0 && kj < a.Sk;
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    uint8_t* sP = smem + L::OFF_P;
+    uint8_t* sdS = smem + L::OFF_DS;
+    uint8_t* sdSN = smem + L::OFF_DSN;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % ST;
+      const int g = t / w.tiles_per_head;
+      const int h = w.kvh * a.group + g;
+      const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
+      // warp-uniform decisions: the tcgen05 loads below need the whole warp
+      bool got = mbar_wait(s_full, t & 1, a.err);
+      if (got && t > 0) got = mbar_wait(mma5_done, (t - 1) & 1, a.err);
+      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      tc_fence_after();
+      const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + s * BM * 4);
+      const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + s * BM * 4);
+      const uint32_t bh = (uint32_t)(w.b * a.H + h);
+      const float* mrow = a.has_mask ? a.mask + w.b * a.msb + h * a.msh + (long long)kj * a.msk
+                                     : nullptr;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BM; c0 += 16) {
+        uint32_t rs[16], rd[16];
+        tmem_ld16(tmem + lane_base + L::T_S + c0, rs);
+        tmem_ld16(tmem + lane_base + L::T_DP + c0, rd);
+        tmem_ld_wait();
+        if (j < 0) continue;  // lane holds no key row (M = 64 layout)
+        float pm[16], ds[16];
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int q = q0 + c0 + c;
+          bool vis = (q < a.Sq) && key_ok;
+          const long long qa = (long long)q + a.causal_offset;
+          if (a.causal) vis = vis && ((long long)kj <= qa);
+          if (a.window > 0) {
+            const long long dist = qa >= kj ? qa - kj : kj - qa;
+            vis = vis && (dist < a.window);
+          }
+          float bias = 0.f;
+          if (a.has_mask && vis) {
+            const float m = __ldg(mrow + (long long)q * a.msq);
+            vis = m > -1.0e30f;
+            bias = m * kLog2e;
+          }
+          const float x = fmaf(__uint_as_float(rs[c]), a.scale_log2e, bias - sLSE[c0 + c]);
+          const float p = vis ? ex2_approx(x) : 0.f;
+          float mult = 1.f;
+          if (a.dropout) {
+            // one Philox call per 4 consecutive queries of this key
+            if ((c & 3) == 0) {
+              const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u, a.seed_lo,
+                                              a.seed_hi);
+              words[0] = r.w[0];
+              words[1] = r.w[1];
+              words[2] = r.w[2];
+              words[3] = r.w[3];
+            }
+            mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
+          }
+          const float dpv = __uint_as_float(rd[c]) * mult;
+          pm[c] = p * mult;
+          ds[c] = a.scale * p * (dpv - sDelta[c0 + c]);
+        }
+        // 16 columns of row j into the swizzled P^T / dS'^T tiles [BN rows][BM]
+        const int blk = c0 / W;
+        const int pos = (c0 % W) * E;
+        if constexpr (BF16) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
+            st_shared_v4(smem_u32(sP + off), pack_bf16(pm[h2 * 8 + 0], pm[h2 * 8 + 1]),
+                         pack_bf16(pm[h2 * 8 + 2], pm[h2 * 8 + 3]),
+                         pack_bf16(pm[h2 * 8 + 4], pm[h2 * 8 + 5]),
+                         pack_bf16(pm[h2 * 8 + 6], pm[h2 * 8 + 7]));
+            st_shared_v4(smem_u32(sdS + off), pack_bf16(ds[h2 * 8 + 0], ds[h2 * 8 + 1]),
+                         pack_bf16(ds[h2 * 8 + 2], ds[h2 * 8 + 3]),
+                         pack_bf16(ds[h2 * 8 + 4], ds[h2 * 8 + 5]),
+                         pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
+          }
+        } else {
+#pragma unroll
+          for (int h4 = 0; h4 < 4; ++h4) {
+            const uint32_t off = sw_off(blk, BN, j, pos + h4 * 16);
+            st_shared_v4(smem_u32(sP + off), to_tf32(pm[h4 * 4 + 0]), to_tf32(pm[h4 * 4 + 1]),
+                         to_tf32(pm[h4 * 4 + 2]), to_tf32(pm[h4 * 4 + 3]));
+            st_shared_v4(smem_u32(sdS + off), to_tf32(ds[h4 * 4 + 0]), to_tf32(ds[h4 * 4 + 1]),
+                         to_tf32(ds[h4 * 4 + 2]), to_tf32(ds[h4 * 4 + 3]));
+          }
+          if constexpr (L::KMAJ) {
+            // dS' also as [BM rows (queries)][BN keys] for GEMM5's K-major operand
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const uint32_t off = sw_off(j / W, BM, c0 + c, (j % W) * 4);
+              st_shared_b32(smem_u32(sdSN + off), to_tf32(ds[c]));
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // --------------------------------------------------------- dK / dV epilogue
+    bool have = ok && T > 0;
+    if (have) {
+      have = !__any_sync(0xffffffffu, !mbar_wait(acc_done, 0, a.err));
+      tc_fence_after();
+    }
+    if (have || T == 0) {
+      const long long off = row_offset(a.layout, w.b, w.kvh, key_ok ? kj : 0, a.Hkv, a.Sk, D);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t rv[16], rk[16];
+        if (have) {  // whole warps: tcgen05.ld is warp-collective
+          tmem_ld16(tmem + lane_base + L::T_DV + c0, rv);
+          tmem_ld16(tmem + lane_base + L::T_DK + c0, rk);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) rv[c] = rk[c] = 0u;
+        }
+        if (!key_ok) continue;
+        if constexpr (BF16) {
+          uint4* dv = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dV) + off + c0);
+          uint4* dk = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dK) + off + c0);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = h2 * 8;
+            dv[h2] = make_uint4(pack_bf16(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1])),
+                                pack_bf16(__uint_as_float(rv[c + 2]), __uint_as_float(rv[c + 3])),
+                                pack_bf16(__uint_as_float(rv[c + 4]), __uint_as_float(rv[c + 5])),
+                                pack_bf16(__uint_as_float(rv[c + 6]), __uint_as_float(rv[c + 7])));
+            dk[h2] = make_uint4(pack_bf16(__uint_as_float(rk[c]), __uint_as_float(rk[c + 1])),
+                                pack_bf16(__uint_as_float(rk[c + 2]), __uint_as_float(rk[c + 3])),
+                                pack_bf16(__uint_as_float(rk[c + 4]), __uint_as_float(rk[c + 5])),
+                                pack_bf16(__uint_as_float(rk[c + 6]), __uint_as_float(rk[c + 7])));
+          }
+        } else {
+          uint4* dv = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.dV) + off + c0);
+          uint4* dk = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.dK) + off + c0);
+#pragma unroll
+          for (int h4 = 0; h4 < 4; ++h4) {
+            dv[h4] = make_uint4(rv[h4 * 4], rv[h4 * 4 + 1], rv[h4 * 4 + 2], rv[h4 * 4 + 3]);
+            dk[h4] = make_uint4(rk[h4 * 4], rk[h4 * 4 + 1], rk[h4 * 4 + 2], rk[h4 * 4 + 3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ group
+    const int r = acc_row<L::M5>((warp - 8) * 32 + lane);  // accumulator row, or -1
+    const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
+    for (int t = 0; t < T; ++t) {
+      const int g = t / w.tiles_per_head;
+      const int h = w.kvh * a.group + g;
+      const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
+      if (__any_sync(0xffffffffu, !mbar_wait(mma5_done, t & 1, a.err))) break;
+      tc_fence_after();
+      float v[L::N5];
+#pragma unroll
+      for (int c0 = 0; c0 < L::N5; c0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tmem + lane_base + L::T_DQ + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c0 + c] = __uint_as_float(rr[c]);
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      if constexpr (L::DQT) {
+        // dQ^T: row r = d, columns = queries of the tile
+        if (r >= 0 && r < D) {
+          float* base = a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D) + r;
+          const long long rstride = a.layout == 0 ? D : (long long)a.H * D;
+          const int nq = min(BM, a.Sq - q0);
+#pragma unroll
+          for (int c = 0; c < BM; ++c)
+            if (c < nq) atomicAdd(base + c * rstride, v[c]);
+        }
+      } else {
+        // dQ: row r = query of the tile, columns = d
+        const int q = q0 + r;
+        if (r >= 0 && q < a.Sq) {
+          float4* dst =
+              reinterpret_cast<float4*>(a.dq_acc + row_offset(a.layout, w.b, h, q, a.H, a.Sq, D));
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c)
+            atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    // products still in flight (only on the unwinding path) must finish first
+    if (T > 0) drain_wait(final_bar, 0);
+    tc_fence_after();
+    tmem_dealloc(tmem, L::T_ALLOC);
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t launch_impl(const TileMaps& m, const TileArgs& a, cudaStream_t stream) {
+  using L = Layout<BF16, D>;
+  auto kern = dkdv_kernel<BF16, D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = a.n_kv_tiles * a.B * a.Hkv;
+  kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int dkdv_block_m(int dtype, int head_dim) {
+  if (dtype == ATTN_BF16) return head_dim == 64 ? Cfg<true, 64>::BM : Cfg<true, 128>::BM;
+  return head_dim == 64 ? Cfg<false, 64>::BM : Cfg<false, 128>::BM;
+}
+
+int dkdv_block_n(int dtype, int head_dim) {
+  if (dtype == ATTN_BF16) return head_dim == 64 ? Cfg<true, 64>::BN : Cfg<true, 128>::BN;
+  return head_dim == 64 ? Cfg<false, 64>::BN : Cfg<false, 128>::BN;
+}
+
+cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,
+                        cudaStream_t stream) {
+  if (p.dtype == ATTN_BF16) {
+    return p.head_dim == 64 ? launch_impl<true, 64>(maps, a, stream)
+                            : launch_impl<true, 128>(maps, a, stream);
+  }
+  return p.head_dim == 64 ? launch_impl<false, 64>(maps, a, stream)
+                          : launch_impl<false, 128>(maps, a, stream);
+}
+
+}  // namespace attnbwd

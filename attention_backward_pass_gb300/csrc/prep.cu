@@ -1,0 +1,202 @@
+// Memory-bound helper kernels of the backward pass.
+//
+//  prep_kernel      Delta_i = dO_i . O_i (the Metal page's "D = rowsum(dO * O)",
+//                   the WGSL page's delta4 sum), LSE2_i = LSE_i * log2(e) for
+//                   the tile kernel's exp2, padding rows (Delta 0, LSE2 +inf so
+//                   P = 0), and zeroing of the fp32 dQ accumulator row.  One
+//                   group of D*esize/16 threads per row, 16-byte loads,
+//                   shuffle reduction inside the group.
+//  transpose        fp32 [B,H,S,D] / [B,S,H,D] -> [B*H][D][S_pad], the
+//                   query- and key-contiguous copies the TF32 products read
+//                   (the tensor cores take TF32 operands K-major only).
+//  dq_convert       fp32 dQ accumulator -> bf16 dQ (round to nearest even).
+//  dropout_mask     the keep mask of one (b, h) slice, for bit-exact tests.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "philox.cuh"
+
+namespace attnbwd {
+
+namespace {
+
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) prep_kernel(const void* __restrict__ O,
+                                                   const void* __restrict__ dO,
+                                                   const float* __restrict__ LSE,
+                                                   float* __restrict__ delta,
+                                                   float* __restrict__ lse2,
+                                                   float* __restrict__ dq_acc, int B, int H,
+                                                   int Sq, int sq_pad, int layout) {
+  constexpr int E = BF16 ? 2 : 4;
+  constexpr int G = D * E / 16;  // threads per row
+  constexpr int ROWS = 256 / G;
+  const int sub = threadIdx.x % G;
+  const long long r = (long long)blockIdx.x * ROWS + threadIdx.x / G;
+  const long long nrows = (long long)B * H * sq_pad;
+  // nrows is a multiple of kRowPad (>= ROWS), so every launched row exists and
+  // no lane leaves before the group shuffle below
+  if (r >= nrows) return;
+  const int i = (int)(r % sq_pad);
+  const int bh = (int)(r / sq_pad);
+  const int b = bh / H, h = bh % H;
+  float acc = 0.f;
+  long long off = 0;
+  if (i < Sq) {
+    off = row_offset(layout, b, h, i, H, Sq, D);
+    if constexpr (BF16) {
+      const uint4 o = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(O) + off)[sub];
+      const uint4 g = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dO) + off)[sub];
+      const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[k]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[k]));
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+    } else {
+      const float4 o = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(O) + off)[sub];
+      const float4 g = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(dO) + off)[sub];
+      acc = fmaf(o.x, g.x, acc);
+      acc = fmaf(o.y, g.y, acc);
+      acc = fmaf(o.z, g.z, acc);
+      acc = fmaf(o.w, g.w, acc);
+    }
+    // zero this row of the dQ accumulator (D fp32 = D/4 float4 over G threads)
+    float4* zq = reinterpret_cast<float4*>(dq_acc + off);
+#pragma unroll
+    for (int c = sub; c < D / 4; c += G) zq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int m = G / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, G);
+  if (sub == 0) {
+    const long long w = (long long)bh * sq_pad + i;
+    if (i < Sq) {
+      delta[w] = acc;
+      lse2[w] = LSE[(long long)bh * Sq + i] * kLog2e;
+    } else {
+      delta[w] = 0.f;
+      lse2[w] = __int_as_float(0x7f800000);  // +inf: P = exp2(x - inf) = 0
+    }
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t prep_impl(const attn_bwd_params& p, const void* O, const void* dO, const float* LSE,
+                      float* delta, float* lse2, int sq_pad, float* dq_acc, cudaStream_t stream) {
+  constexpr int G = D * (BF16 ? 2 : 4) / 16;
+  constexpr int ROWS = 256 / G;
+  const long long nrows = (long long)p.batch * p.num_heads * sq_pad;
+  const long long blocks = (nrows + ROWS - 1) / ROWS;
+  prep_kernel<BF16, D><<<(unsigned)blocks, 256, 0, stream>>>(
+      O, dO, LSE, delta, lse2, dq_acc, p.batch, p.num_heads, p.seq_q, sq_pad, p.layout);
+  return cudaGetLastError();
+}
+
+// 32 x 32 tiles through padded shared memory: coalesced reads along d,
+// coalesced writes along s.
+__global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ X,
+                                                        float* __restrict__ XT, int Hx, int S,
+                                                        int D, int s_pad, int layout) {
+  __shared__ float tile[32][33];
+  const int s0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
+  const int bh = blockIdx.z;
+  const int b = bh / Hx, h = bh % Hx;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int s = s0 + ty + 8 * k;
+    tile[ty + 8 * k][tx] = s < S ? X[row_offset(layout, b, h, s, Hx, S, D) + d0 + tx] : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int d = d0 + ty + 8 * k;
+    const int s = s0 + tx;
+    if (s < s_pad) {
+      // rounded to TF32 (nearest, ties away) once here: these copies only
+      // feed TF32 products, which would otherwise truncate the fp32 values
+      uint32_t r;
+      asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(tile[tx][ty + 8 * k]));
+      XT[((long long)bh * D + d) * s_pad + s] = __uint_as_float(r);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src,
+                                                         uint2* __restrict__ dst, long long n4) {
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n4;
+       k += (long long)gridDim.x * blockDim.x) {
+    const float4 v = src[k];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    dst[k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
+__global__ void __launch_bounds__(256) dropout_mask_kernel(uint8_t* __restrict__ keep, int Sq,
+                                                           int Sk, uint32_t bh, uint32_t seed_lo,
+                                                           uint32_t seed_hi, uint32_t threshold) {
+  const long long n = (long long)Sq * Sk;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n;
+       k += (long long)gridDim.x * blockDim.x) {
+    const uint32_t i = (uint32_t)(k / Sk), j = (uint32_t)(k % Sk);
+    const Philox4 r = philox4x32_10(i >> 2, j, bh, 0u, seed_lo, seed_hi);
+    keep[k] = r.w[i & 3] >= threshold ? 1 : 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const attn_bwd_params& p, const void* O, const void* dO, const float* LSE,
+                        float* delta, float* lse2, int sq_pad, float* dq_acc,
+                        cudaStream_t stream) {
+  const bool bf = p.dtype == ATTN_BF16;
+  if (p.head_dim == 64)
+    return bf ? prep_impl<true, 64>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream)
+              : prep_impl<false, 64>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream);
+  return bf ? prep_impl<true, 128>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream)
+            : prep_impl<false, 128>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream);
+}
+
+cudaError_t launch_transpose(const float* X, float* XT, int B, int Hx, int S, int D, int s_pad,
+                             int layout, cudaStream_t stream) {
+  dim3 grid((s_pad + 31) / 32, D / 32, B * Hx);
+  transpose_kernel<<<grid, 256, 0, stream>>>(X, XT, Hx, S, D, s_pad, layout);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, void* dQ,
+                              cudaStream_t stream) {
+  const long long n4 = (long long)p.batch * p.num_heads * p.seq_q * p.head_dim / 4;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dQ), n4);
+  return cudaGetLastError();
+}
+
+// keep iff word >= T, T = min(floor(p * 2^32), 2^32 - 1), computed in fp64
+uint32_t dropout_threshold(float prob) {
+  if (!(prob > 0.f)) return 0u;
+  double t = (double)prob * 4294967296.0;
+  if (t >= 4294967295.0) return 0xFFFFFFFFu;
+  return (uint32_t)t;
+}
+
+cudaError_t launch_dropout_mask(const attn_bwd_params& p, int b, int h, uint8_t* keep,
+                                cudaStream_t stream) {
+  const long long n = (long long)p.seq_q * p.seq_k;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks < 1) blocks = 1;
+  dropout_mask_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      keep, p.seq_q, p.seq_k, (uint32_t)(b * p.num_heads + h), (uint32_t)(p.seed & 0xFFFFFFFFu),
+      (uint32_t)(p.seed >> 32), dropout_threshold(p.dropout_prob));
+  return cudaGetLastError();
+}
+
+}  // namespace attnbwd

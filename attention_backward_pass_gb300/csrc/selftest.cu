@@ -1,0 +1,162 @@
+// Tensor-core self test: one CTA computes C = A * B^T with tcgen05.mma from
+// operands staged in 128-byte-swizzled shared memory, in K-major or MN-major
+// form, and reads the accumulator back from tensor memory.  This is the
+// building block every tile kernel of the library relies on (same descriptor
+// and swizzle helpers), checked in isolation against a CPU product.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_bwd.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attnbwd {
+
+namespace {
+
+constexpr int kMaxDim = 256;
+
+// Byte offset of element `pos` (0..W-1) of row `row` in column block `blk`
+// of a 128-byte-swizzled tile with `rows` rows per block.
+__device__ __forceinline__ uint32_t sw128_offset(int blk, int rows, int row, int pos_bytes) {
+  const int chunk = (pos_bytes >> 4) ^ (row & 7);
+  return (uint32_t)(blk * rows * 128 + row * 128 + chunk * 16 + (pos_bytes & 15));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, int a_mn, int b_mn,
+                                                           const void* __restrict__ A,
+                                                           const void* __restrict__ B,
+                                                           float* __restrict__ C,
+                                                           float* __restrict__ dump,
+                                                           unsigned int* err) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  constexpr int E = sizeof(T);
+  constexpr int W = 128 / E;  // elements per 128-byte row segment
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                  // up to 128 x 128 fp32 = 64 KB
+  uint8_t* sB = smem + 65536;                          // up to 256 x 128 fp32 = 128 KB
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+
+  const T* gA = reinterpret_cast<const T*>(A);
+  const T* gB = reinterpret_cast<const T*>(B);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+
+  // Stage A [M][K] and B [N][K].  K-major: blocks along K, rows = M (or N).
+  // MN-major: blocks along M (or N), rows = K.
+  for (int idx = tid; idx < M * K; idx += blockDim.x) {
+    const int m = idx / K, k = idx % K;
+    uint32_t off = a_mn ? sw128_offset(m / W, K, k, (m % W) * E)
+                        : sw128_offset(k / W, M, m, (k % W) * E);
+    *reinterpret_cast<T*>(sA + off) = gA[idx];
+  }
+  for (int idx = tid; idx < N * K; idx += blockDim.x) {
+    const int n = idx / K, k = idx % K;
+    uint32_t off = b_mn ? sw128_offset(n / W, K, k, (n % W) * E)
+                        : sw128_offset(k / W, N, n, (k % W) * E);
+    *reinterpret_cast<T*>(sB + off) = gB[idx];
+  }
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  uint32_t ncols = 32;
+  while ((int)ncols < N) ncols <<= 1;
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 1 && elect_one_sync()) {
+    const uint32_t idesc = make_idesc(BF16, M, N, a_mn != 0, b_mn != 0);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+    constexpr int KSTEP = 32 / E;  // elements of K per instruction (32 bytes)
+    for (int ks = 0; ks < K / KSTEP; ++ks) {
+      uint64_t ad, bd;
+      if (a_mn) {
+        ad = sw128_desc(a0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u);
+      } else {
+        const int kb = ks * 32;
+        ad = sw128_desc(a0 + (kb / 128) * M * 128 + (kb % 128), 16u, 1024u);
+      }
+      if (b_mn) {
+        bd = sw128_desc(b0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u);
+      } else {
+        const int kb = ks * 32;
+        bd = sw128_desc(b0 + (kb / 128) * N * 128 + (kb % 128), 16u, 1024u);
+      }
+      mma_ss<BF16>(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+    }
+    mma_commit(&bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, err);
+  tc_fence_after();
+
+  // Every warp reads its 32-lane sub-partition: lane = warp*32 + (tid & 31).
+  const int lane = warp * 32 + (tid & 31);
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+      tmem_ld_wait();
+      for (int j = 0; j < 16; ++j) {
+        const float v = __uint_as_float(r[j]);
+        if (dump) dump[lane * N + c0 + j] = v;
+        int row = -1;
+        if (M == 128) {
+          row = lane;
+        } else if ((lane & 31) < 16) {  // M = 64: 16 lanes per sub-partition
+          row = (lane >> 5) * 16 + (lane & 15);
+        }
+        if (row >= 0 && row < M) C[row * N + c0 + j] = v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+}  // namespace
+
+attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, const void* A,
+                                const void* B, float* C, float* dump, cudaStream_t stream) {
+  const int W = dtype == ATTN_BF16 ? 64 : 32;
+  if (!(M == 64 || M == 128)) return ATTN_ERR_INVALID;
+  if (N < 16 || N > kMaxDim || N % 16 != 0) return ATTN_ERR_INVALID;
+  if (K < W || K > 128 || K % W != 0) return ATTN_ERR_INVALID;
+  if ((a_mn && M % W) || (b_mn && N % W)) return ATTN_ERR_INVALID;
+  if (!A || !B || !C) return ATTN_ERR_INVALID;
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  const size_t smem = 1024 + 65536 + 131072;
+  cudaError_t e;
+  if (dtype == ATTN_BF16) {
+    e = cudaFuncSetAttribute(selftest_mma_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) {
+      selftest_mma_kernel<true><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, A, B, C, dump, err);
+      e = cudaGetLastError();
+    }
+  } else {
+    e = cudaFuncSetAttribute(selftest_mma_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) {
+      selftest_mma_kernel<false><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, A, B, C, dump, err);
+      e = cudaGetLastError();
+    }
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attnbwd

@@ -1,0 +1,130 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI
+and the fp64 oracle on the same seeded inputs, and compare.
+
+Metric (per output tensor, over the compared slice):
+    max |gpu - oracle| / max |oracle|
+Bars: 2e-3 for fp32 I/O (TF32 tensor-core products), 2e-2 for bf16 I/O.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from attention_backward_pass_gb300 import workloads as W
+from oracle import attention as OA
+from oracle import decode as OD
+
+TOL = {W.DTYPE_F32: 2e-3, W.DTYPE_BF16: 2e-2}
+
+
+def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    gpu = np.asarray(gpu, dtype=np.float64)
+    denom = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if denom == 0.0:
+        return float(np.max(np.abs(gpu))) if gpu.size else 0.0
+    return float(np.max(np.abs(gpu - ref))) / denom
+
+
+def _torch_io(x, dtype, device):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+    return t.to(torch.bfloat16) if dtype == W.DTYPE_BF16 else t
+
+
+def make_case(p, seed, groups=None, fill_lse=1.0e4):
+    """Seeded inputs plus O and LSE from the oracle forward, rounded once to
+    the I/O dtype (O) and fp32 (LSE).  When ``groups`` is given, the forward
+    runs only for those (b, kv-head) groups; the other heads get random O and
+    a large LSE (their outputs are not compared)."""
+    Q, K, V, dO, mask = W.make_inputs(p, seed)
+    O, LSE = OA.forward(p, Q, K, V, mask, groups=groups)
+    if groups is not None:
+        rng = np.random.default_rng(seed + 1)
+        G = p.num_heads // p.num_kv_heads
+        done = np.zeros((p.batch, p.num_heads), dtype=bool)
+        for b, g in groups:
+            done[b, g * G:(g + 1) * G] = True
+        for b in range(p.batch):
+            for h in range(p.num_heads):
+                if not done[b, h]:
+                    LSE[b, h] = fill_lse
+                    if p.layout == W.LAYOUT_BHSD:
+                        O[b, h] = rng.standard_normal(O[b, h].shape)
+                    else:
+                        O[b, :, h] = rng.standard_normal(O[b, :, h].shape)
+    O = W.round_io(O.astype(np.float32), p.dtype)
+    LSE = LSE.astype(np.float32)
+    return dict(Q=Q, K=K, V=V, dO=dO, mask=mask, O=O, LSE=LSE)
+
+
+def run_gpu(p, case, device="cuda", repeat=1):
+    """Runs attn_bwd through the C ABI; returns fp64 numpy dQ, dK, dV."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    t = {k: _torch_io(case[k], p.dtype, device) for k in ("Q", "K", "V", "O", "dO")}
+    lse = torch.from_numpy(case["LSE"]).to(device)
+    mask = torch.from_numpy(case["mask"]).to(device) if case["mask"] is not None else None
+    tdt = torch.bfloat16 if p.dtype == W.DTYPE_BF16 else torch.float32
+    dQ = torch.full(p.q_shape(), float("nan"), dtype=tdt, device=device)
+    dK = torch.full(p.kv_shape(), float("nan"), dtype=tdt, device=device)
+    dV = torch.full(p.kv_shape(), float("nan"), dtype=tdt, device=device)
+    ws = ab.alloc_workspace(p, device)
+    ws.fill_(0xFF)  # contents on entry must not matter
+    for _ in range(repeat):
+        ab.attn_bwd(p, t["Q"], t["K"], t["V"], t["O"], t["dO"], lse, mask, dQ, dK, dV, ws)
+    torch.cuda.synchronize()
+    assert ab.check_device_error() == 0
+    return [x.float().cpu().numpy().astype(np.float64) for x in (dQ, dK, dV)]
+
+
+def oracle_grads(p, case, groups=None):
+    f = lambda x: x.astype(np.float64)  # noqa: E731
+    return OA.backward(p, f(case["Q"]), f(case["K"]), f(case["V"]), f(case["O"]), f(case["dO"]),
+                       case["LSE"].astype(np.float64), case["mask"], groups=groups)
+
+
+def select_groups(p, arr, groups, side):
+    """Stack the slices of `arr` that belong to the (b, kv-head) groups."""
+    G = p.num_heads // p.num_kv_heads
+    out = []
+    for b, g in groups:
+        heads = range(g * G, (g + 1) * G) if side == "q" else [g]
+        for h in heads:
+            out.append(arr[b, h] if p.layout == W.LAYOUT_BHSD else arr[b, :, h])
+    return np.stack(out)
+
+
+def compare(p, case, groups=None, repeat=1):
+    """Returns {name: rel_err} for dQ, dK, dV (on the sampled groups if given)."""
+    gpu = run_gpu(p, case, repeat=repeat)
+    ref = oracle_grads(p, case, groups)
+    errs = {}
+    for name, g, r, side in zip(("dQ", "dK", "dV"), gpu, ref, ("q", "k", "k")):
+        assert np.all(np.isfinite(g if groups is None else select_groups(p, g, groups, side))), name
+        if groups is None:
+            errs[name] = rel_err(g, r)
+        else:
+            errs[name] = rel_err(select_groups(p, g, groups, side),
+                                 select_groups(p, r, groups, side))
+    return errs
+
+
+def decode_case(p, seed):
+    k, v, d_out, logits = W.make_decode_inputs(p, seed)
+    probs = OD.softmax_rows(logits).astype(np.float32)
+    return dict(k=k, v=v, d_out=d_out, probs=probs)
+
+
+def run_decode_gpu(p, case, device="cuda", repeat=1):
+    import torch
+    import attention_backward_pass_gb300 as ab
+    t = {k: torch.from_numpy(np.ascontiguousarray(case[k])).to(device)
+         for k in ("k", "v", "d_out", "probs")}
+    d_scores = torch.full((p.num_seqs, p.n_heads, p.history_len), float("nan"), device=device)
+    d_q = torch.full((p.num_seqs, p.n_heads, p.head_dim), float("nan"), device=device)
+    ws = ab.alloc_decode_workspace(p, device)
+    for _ in range(repeat):
+        ab.attn_bwd_decode(p, t["k"], t["v"], t["probs"], t["d_out"], d_scores, d_q, ws)
+    torch.cuda.synchronize()
+    assert ab.check_device_error() == 0
+    return d_scores.cpu().numpy().astype(np.float64), d_q.cpu().numpy().astype(np.float64)

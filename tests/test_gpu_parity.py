@@ -1,0 +1,123 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs.
+
+Small problems span several tiles and a ragged tail and are compared in full;
+the full-size workloads are compared on seeded (batch, kv-head) groups.
+Bars: max|err|/max|ref| <= 2e-3 (fp32 I/O, TF32 products) and <= 2e-2
+(bf16 I/O); dropout keep masks bit-exact.
+"""
+import numpy as np
+import pytest
+
+from attention_backward_pass_gb300 import workloads as W
+from oracle import decode as OD
+from oracle import philox
+
+from parity_helpers import TOL, compare, decode_case, make_case, rel_err, run_decode_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def P(**kw):
+    base = dict(batch=1, num_heads=2, num_kv_heads=2, seq_q=64, seq_k=64, head_dim=64,
+                scale=0.125)
+    base.update(kw)
+    p = W.AttnProblem(**base)
+    if p.has_mask:
+        p.mask_stride_b, p.mask_stride_h = p.seq_q * p.seq_k, 0
+        p.mask_stride_q, p.mask_stride_k = p.seq_k, 1
+    return p
+
+
+SMALL = {
+    "tiny": W.tiny(),
+    "causal_ragged_d64": P(seq_q=300, seq_k=300, causal=1),
+    "noncausal_rect_d64": P(seq_q=200, seq_k=333),
+    "gqa_window_bshd_d128": P(num_heads=4, num_kv_heads=2, seq_q=384, seq_k=384, head_dim=128,
+                              causal=1, window=100, layout=W.LAYOUT_BSHD,
+                              scale=1 / np.sqrt(128)),
+    "window_only_offset": P(seq_q=150, seq_k=260, window=40, causal_offset=60),
+    "mask_dropout_offset": P(seq_q=200, seq_k=520, causal=1, causal_offset=320, has_mask=1,
+                             dropout_prob=0.1, seed=0x5EED0004),
+    "single_query_key": P(seq_q=1, seq_k=1),
+    "empty_rows": P(seq_q=100, seq_k=90, window=5, causal_offset=80),
+}
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_parity(name, dtype):
+    import copy
+    p = copy.copy(SMALL[name])
+    p.dtype = dtype
+    case = make_case(p, seed=1234)
+    errs = compare(p, case)
+    assert all(e <= TOL[dtype] for e in errs.values()), errs
+
+
+def test_keep_mask_bit_exact():
+    import torch
+    import attention_backward_pass_gb300 as ab
+    p = W.masked_dropout()
+    for b, h in [(0, 0), (1, 15), (0, 7)]:
+        keep = torch.empty((p.seq_q, p.seq_k), dtype=torch.uint8, device="cuda")
+        ab.dropout_keep_mask(p, b, h, keep)
+        ref = philox.keep_mask(p.seed, b * p.num_heads + h, p.seq_q, p.seq_k, p.dropout_prob)
+        assert np.array_equal(keep.cpu().numpy().astype(bool), ref)
+
+
+def test_repeat_calls_overwrite():
+    p = SMALL["causal_ragged_d64"]
+    case = make_case(p, seed=5)
+    errs = compare(p, case, repeat=3)
+    assert all(e <= TOL[p.dtype] for e in errs.values()), errs
+
+
+# ------------------------------------------------------------- full sizes
+
+FULL = {
+    "tiny": (W.tiny, None),
+    "causal_mha": (W.causal_mha, [(0, 0), (3, 15), (2, 6)]),
+    "gqa_window_f32": (lambda: W.gqa_window(W.DTYPE_F32), [(0, 0), (1, 7)]),
+    "gqa_window_bf16": (lambda: W.gqa_window(W.DTYPE_BF16), [(1, 3)]),
+    "masked_dropout": (W.masked_dropout, [(0, 0), (1, 9)]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_full_size_sampled(name):
+    make, groups = FULL[name]
+    p = make()
+    seed = W.WORKLOADS.get(name, (None, 2))[1]
+    case = make_case(p, seed=seed, groups=groups)
+    errs = compare(p, case, groups=groups)
+    assert all(e <= TOL[p.dtype] for e in errs.values()), errs
+
+
+# ------------------------------------------------------------- decode
+
+DECODE = {
+    "small_g8_d256": W.DecodeProblem(2, 8, 1, 256, 300),
+    "g2_kv2_d64_ragged": W.DecodeProblem(3, 4, 2, 64, 17),
+    "g1_d128": W.DecodeProblem(2, 4, 4, 128, 1000),
+    "g16_d64": W.DecodeProblem(1, 16, 1, 64, 77),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE))
+def test_decode_parity(name):
+    p = DECODE[name]
+    case = decode_case(p, seed=7)
+    ds, dq = run_decode_gpu(p, case)
+    rds, rdq = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"])
+    assert rel_err(ds, rds) <= 2e-3 and rel_err(dq, rdq) <= 2e-3, (rel_err(ds, rds),
+                                                                    rel_err(dq, rdq))
+
+
+def test_decode_full_size_sampled():
+    p = W.decode()
+    case = decode_case(p, seed=4)
+    ds, dq = run_decode_gpu(p, case, repeat=2)
+    seqs = [0, 31, 63]
+    rds, rdq = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"], seqs=seqs)
+    assert rel_err(ds[seqs], rds[seqs]) <= 2e-3
+    assert rel_err(dq[seqs], rdq[seqs]) <= 2e-3
