@@ -58,6 +58,12 @@ _SIGS = {
     "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdParams)]),
     "attn_bwd": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_prepare": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P, _P, _P,
+                                        ctypes.c_size_t, _P]),
+    "attn_bwd_tiles": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_finish": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, ctypes.c_size_t,
+                                       _P]),
     "attn_bwd_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdDecodeParams)]),
     "attn_bwd_decode": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P, _P, _P,
                                        _P, _P, ctypes.c_size_t, _P]),
@@ -146,6 +152,39 @@ def attn_bwd(p, Q, K, V, O, dO, LSE, mask, dQ, dK, dV, workspace, stream=None):
                       ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                       _stream_ptr(stream))
     _check("attn_bwd", st)
+
+
+def _wsb(workspace):
+    return ctypes.c_size_t(workspace.numel() * workspace.element_size())
+
+
+def attn_bwd_prepare(p, Q, K, O, dO, LSE, dQ, workspace, stream=None):
+    """Stage 1 of attn_bwd: Delta, LSE*log2(e), dQ accumulator reset, transposes."""
+    st = load_library().attn_bwd_prepare(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(O),
+                                         _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(workspace),
+                                         _wsb(workspace), _stream_ptr(stream))
+    _check("attn_bwd_prepare", st)
+
+
+def attn_bwd_tiles(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, stream=None):
+    """Stage 2 of attn_bwd: the fused tcgen05 tile kernel."""
+    st = load_library().attn_bwd_tiles(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(V),
+                                       _ptr(dO), _ptr(mask), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                       _ptr(workspace), _wsb(workspace), _stream_ptr(stream))
+    _check("attn_bwd_tiles", st)
+
+
+def attn_bwd_finish(p, dQ, workspace, stream=None):
+    """Stage 3 of attn_bwd: bf16 dQ from the fp32 accumulator (no-op for fp32)."""
+    st = load_library().attn_bwd_finish(ctypes.byref(make_params(p)), _ptr(dQ), _ptr(workspace),
+                                        _wsb(workspace), _stream_ptr(stream))
+    _check("attn_bwd_finish", st)
+
+
+def kernels_per_call(p) -> int:
+    """Kernels one attn_bwd call launches (prep, 3 transposes for fp32, tile
+    kernel, bf16 dQ conversion)."""
+    return 1 + (3 if p.dtype == ATTN_F32 else 0) + 1 + (1 if p.dtype == ATTN_BF16 else 0)
 
 
 def make_decode_params(p) -> AttnBwdDecodeParams:

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "attn_bwd.h"
@@ -177,44 +178,86 @@ size_t attn_bwd_workspace_size(const attn_bwd_params* p) {
   return ws_layout(*p).total;
 }
 
-attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
-                     const void* O, const void* dO, const float* LSE, const float* mask,
-                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
-                     void* stream_v) {
+namespace {
+
+struct Plan {
+  WsLayout wl;
+  float *delta, *lse2, *dq_acc, *qt, *dot, *kt;
+};
+
+attn_status make_plan(const attn_bwd_params* p, void* dQ, void* workspace, size_t workspace_bytes,
+                      Plan* pl) {
   attn_status st = validate(p);
   if (st != ATTN_OK) return st;
-  const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
-  for (const void* q : ptrs)
-    if (!q || !aligned16(q)) return ATTN_ERR_INVALID;
-  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
-  const WsLayout wl = ws_layout(*p);
+  if (!dQ || !aligned16(dQ)) return ATTN_ERR_INVALID;
+  pl->wl = ws_layout(*p);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
-      workspace_bytes < wl.total)
+      workspace_bytes < pl->wl.total)
     return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  pl->delta = reinterpret_cast<float*>(ws + pl->wl.delta);
+  pl->lse2 = reinterpret_cast<float*>(ws + pl->wl.lse2);
+  pl->dq_acc = p->dtype == ATTN_BF16 ? reinterpret_cast<float*>(ws + pl->wl.dq_acc)
+                                     : reinterpret_cast<float*>(dQ);
+  pl->qt = reinterpret_cast<float*>(ws + pl->wl.qt);
+  pl->dot = reinterpret_cast<float*>(ws + pl->wl.dot);
+  pl->kt = reinterpret_cast<float*>(ws + pl->wl.kt);
+  return ATTN_OK;
+}
+
+bool all_aligned(std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return false;
+  return true;
+}
+
+}  // namespace
+
+attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
+                             const void* O, const void* dO, const float* LSE, void* dQ,
+                             void* workspace, size_t workspace_bytes, void* stream_v) {
+  Plan pl;
+  attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
+  if (st != ATTN_OK) return st;
+  if (!all_aligned({Q, K, O, dO, LSE})) return ATTN_ERR_INVALID;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  if (launch_prep(*p, O, dO, LSE, pl.delta, pl.lse2, pl.wl.sq_pad, pl.dq_acc, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (p->dtype != ATTN_BF16 &&
+      (launch_transpose(static_cast<const float*>(Q), pl.qt, p->batch, p->num_heads, p->seq_q,
+                        p->head_dim, pl.wl.sq_pad, p->layout, stream) != cudaSuccess ||
+       launch_transpose(static_cast<const float*>(dO), pl.dot, p->batch, p->num_heads, p->seq_q,
+                        p->head_dim, pl.wl.sq_pad, p->layout, stream) != cudaSuccess ||
+       launch_transpose(static_cast<const float*>(K), pl.kt, p->batch, p->num_kv_heads, p->seq_k,
+                        p->head_dim, pl.wl.sk_pad, p->layout, stream) != cudaSuccess))
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                           const void* dO, const float* mask, void* dQ, void* dK, void* dV,
+                           void* workspace, size_t workspace_bytes, void* stream_v) {
+  Plan pl;
+  attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
+  if (st != ATTN_OK) return st;
+  if (!all_aligned({Q, K, V, dO, dK, dV})) return ATTN_ERR_INVALID;
+  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   unsigned int* err = device_error_word();
   if (!err) return ATTN_ERR_CUDA;
-
-  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  float* delta = reinterpret_cast<float*>(ws + wl.delta);
-  float* lse2 = reinterpret_cast<float*>(ws + wl.lse2);
-  float* dq_acc = p->dtype == ATTN_BF16 ? reinterpret_cast<float*>(ws + wl.dq_acc)
-                                        : reinterpret_cast<float*>(dQ);
 
   TileMaps maps;
   memset(&maps, 0, sizeof(maps));
   const int bm = dkdv_block_m(p->dtype, p->head_dim);
   const int bn = dkdv_block_n(p->dtype, p->head_dim);
-  const bool fp32 = p->dtype != ATTN_BF16;
-  float* qt = reinterpret_cast<float*>(ws + wl.qt);
-  float* dot = reinterpret_cast<float*>(ws + wl.dot);
-  float* kt = reinterpret_cast<float*>(ws + wl.kt);
-  if (fp32 && (make_map_t(&maps.qt, qt, p->head_dim, p->seq_q, wl.sq_pad,
-                          p->batch * p->num_heads) != CUDA_SUCCESS ||
-               make_map_t(&maps.dot, dot, p->head_dim, p->seq_q, wl.sq_pad,
-                          p->batch * p->num_heads) != CUDA_SUCCESS ||
-               make_map_t(&maps.kt, kt, p->head_dim, p->seq_k, wl.sk_pad,
-                          p->batch * p->num_kv_heads) != CUDA_SUCCESS))
+  if (p->dtype != ATTN_BF16 &&
+      (make_map_t(&maps.qt, pl.qt, p->head_dim, p->seq_q, pl.wl.sq_pad,
+                  p->batch * p->num_heads) != CUDA_SUCCESS ||
+       make_map_t(&maps.dot, pl.dot, p->head_dim, p->seq_q, pl.wl.sq_pad,
+                  p->batch * p->num_heads) != CUDA_SUCCESS ||
+       make_map_t(&maps.kt, pl.kt, p->head_dim, p->seq_k, pl.wl.sk_pad,
+                  p->batch * p->num_kv_heads) != CUDA_SUCCESS))
     return ATTN_ERR_CUDA;
   if (make_map(&maps.q, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
                bm) != CUDA_SUCCESS ||
@@ -235,7 +278,7 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
   a.Sk = p->seq_k;
   a.D = p->head_dim;
   a.group = p->num_heads / p->num_kv_heads;
-  a.sq_pad = wl.sq_pad;
+  a.sq_pad = pl.wl.sq_pad;
   a.layout = p->layout;
   a.scale = p->scale;
   a.scale_log2e = p->scale * kLog2e;
@@ -253,27 +296,42 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
   a.drop_inv_keep = (float)(1.0 / (1.0 - (double)p->dropout_prob));
   a.seed_lo = (uint32_t)(p->seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(p->seed >> 32);
-  a.lse2 = lse2;
-  a.delta = delta;
-  a.dq_acc = dq_acc;
+  a.lse2 = pl.lse2;
+  a.delta = pl.delta;
+  a.dq_acc = pl.dq_acc;
   a.dK = dK;
   a.dV = dV;
   a.n_kv_tiles = (p->seq_k + bn - 1) / bn;
   a.err = err;
-
-  if (launch_prep(*p, O, dO, LSE, delta, lse2, wl.sq_pad, dq_acc, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (fp32 && (launch_transpose(static_cast<const float*>(Q), qt, p->batch, p->num_heads,
-                                p->seq_q, p->head_dim, wl.sq_pad, p->layout, stream) != cudaSuccess ||
-               launch_transpose(static_cast<const float*>(dO), dot, p->batch, p->num_heads,
-                                p->seq_q, p->head_dim, wl.sq_pad, p->layout, stream) != cudaSuccess ||
-               launch_transpose(static_cast<const float*>(K), kt, p->batch, p->num_kv_heads,
-                                p->seq_k, p->head_dim, wl.sk_pad, p->layout, stream) != cudaSuccess))
-    return ATTN_ERR_CUDA;
   if (launch_dkdv(*p, maps, a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (p->dtype == ATTN_BF16 && launch_dq_convert(*p, dq_acc, dQ, stream) != cudaSuccess)
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
+                            size_t workspace_bytes, void* stream_v) {
+  Plan pl;
+  attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
+  if (st != ATTN_OK) return st;
+  if (p->dtype == ATTN_BF16 &&
+      launch_dq_convert(*p, pl.dq_acc, dQ, reinterpret_cast<cudaStream_t>(stream_v)) !=
+          cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                     const void* O, const void* dO, const float* LSE, const float* mask,
+                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!all_aligned({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID;
+  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
+  st = attn_bwd_prepare(p, Q, K, O, dO, LSE, dQ, workspace, workspace_bytes, stream);
+  if (st != ATTN_OK) return st;
+  st = attn_bwd_tiles(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, workspace_bytes, stream);
+  if (st != ATTN_OK) return st;
+  return attn_bwd_finish(p, dQ, workspace, workspace_bytes, stream);
 }
 
 static attn_status validate_decode(const attn_bwd_decode_params* p) {

@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 attention backward pass (dQ + dK + dV).
+
+One step = one full backward pass (attn_bwd: Delta/LSE prep, the fp32
+transposes, the fused tcgen05 tile kernel and, for bf16, the dQ conversion)
+over one batch of the chosen workload, with inputs resident in HBM.  The
+metric counts 10*D flops per visible (query, key) pair per query head (the
+five dense contractions); recomputation is not credited.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy of
+the workload on its own GPU (weak scaling, no collective on the data path);
+the reported value is the work of all ranks over the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from attention_backward_pass_gb300 import metrics as MET  # noqa: E402
+from attention_backward_pass_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention-backward TFLOP/s (dQ+dK+dV) and % of GB300 dense tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+# nominal dense ratio TF32 : BF16 on GB300 (1.1 vs 2.25 PFLOP/s)
+TF32_OVER_BF16 = 1.1 / 2.25
+
+WORKLOADS = {
+    "causal_mha": (W.causal_mha, 1,
+                   "causal MHA B4 H16 S1024 D64 fp32 [B,H,S,D]"),
+    "gqa_window_f32": (lambda: W.gqa_window(W.DTYPE_F32), 2,
+                       "GQA causal+window1024 B2 Hq32 Hkv8 S4096 D128 fp32 [B,S,H,D]"),
+    "gqa_window_bf16": (lambda: W.gqa_window(W.DTYPE_BF16), 2,
+                        "GQA causal+window1024 B2 Hq32 Hkv8 S4096 D128 bf16 [B,S,H,D]"),
+    "masked_dropout": (W.masked_dropout, 3,
+                       "masked+dropout B2 H16 Sq512 Sk2048 D64 fp32 causal_offset1536 p0.1"),
+    "tiny": (W.tiny, 0, "tiny B1 H2 S64 D64 fp32"),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="causal_mha", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------- inputs
+
+def synth_forward(p, Q, K, V, mask):
+    """O and LSE for the timed backward, from a plain torch forward on the GPU
+    (input synthesis, untimed; no dropout).  Fully masked rows get LSE = 3e38
+    and O = 0, the WGSL page's convention."""
+    import torch
+    dev = Q.device
+    B, H, Hkv = p.batch, p.num_heads, p.num_kv_heads
+    G = H // Hkv
+    O = torch.empty_like(Q)
+    LSE = torch.empty(p.lse_shape(), dtype=torch.float32, device=dev)
+    i = torch.arange(p.seq_q, device=dev)[:, None] + p.causal_offset
+    j = torch.arange(p.seq_k, device=dev)[None, :]
+    allowed = torch.ones(p.seq_q, p.seq_k, dtype=torch.bool, device=dev)
+    if p.causal:
+        allowed &= j <= i
+    if p.window:
+        allowed &= (i - j).abs() < p.window
+    for b in range(B):
+        for h in range(H):
+            kvh = h // G
+            if p.layout == W.LAYOUT_BHSD:
+                q, k, v = Q[b, h].float(), K[b, kvh].float(), V[b, kvh].float()
+            else:
+                q, k, v = Q[b, :, h].float(), K[b, :, kvh].float(), V[b, :, kvh].float()
+            s = p.scale * (q @ k.T)
+            al = allowed
+            if mask is not None:
+                m = mask[b, 0]
+                al = al & (m > -1e30)
+                s = s + torch.where(m > -1e30, m, torch.zeros_like(m))
+            s = s.masked_fill(~al, float("-inf"))
+            lse = torch.logsumexp(s, dim=-1)
+            empty = ~torch.isfinite(lse)
+            P = torch.exp(s - torch.where(empty, torch.zeros_like(lse), lse)[:, None])
+            P = torch.where(al, P, torch.zeros_like(P))
+            o = (P @ v).to(Q.dtype)
+            o[empty] = 0
+            lse = torch.where(empty, torch.full_like(lse, 3.0e38), lse)
+            if p.layout == W.LAYOUT_BHSD:
+                O[b, h] = o
+            else:
+                O[b, :, h] = o
+            LSE[b, h] = lse
+    return O, LSE
+
+
+def device_inputs(p, seed, device):
+    import torch
+    Qn, Kn, Vn, dOn, maskn = W.make_inputs(p, seed)
+    tdt = torch.bfloat16 if p.dtype == W.DTYPE_BF16 else torch.float32
+    to = lambda x: torch.from_numpy(x).to(device).to(tdt)  # noqa: E731
+    Q, K, V, dO = to(Qn), to(Kn), to(Vn), to(dOn)
+    mask = torch.from_numpy(maskn).to(device) if maskn is not None else None
+    O, LSE = synth_forward(p, Q, K, V, mask)
+    return dict(Q=Q, K=K, V=V, O=O, dO=dO, LSE=LSE, mask=mask,
+                numpy=dict(Q=Qn, K=Kn, V=Vn, dO=dOn, mask=maskn))
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            sel = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample_tflops(p, numpy_inputs, O_np, LSE_np, budget_s: float, rng_seed=0):
+    """Time the fp64 oracle on seeded (batch, kv-head) groups until the time
+    budget is used; returns (TFLOP/s scaled to the metric's flop count, groups
+    done, total groups, seconds)."""
+    from oracle import attention as OA
+    groups_all = [(b, g) for b in range(p.batch) for g in range(p.num_kv_heads)]
+    rng = np.random.default_rng(rng_seed)
+    order = rng.permutation(len(groups_all))
+    per_group = MET.counted_flops(p) / len(groups_all)
+    f = lambda x: None if x is None else x.astype(np.float64)  # noqa: E731
+    Q, K, V, dO = (f(numpy_inputs[k]) for k in ("Q", "K", "V", "dO"))
+    mask = numpy_inputs["mask"]
+    done, t_total = 0, 0.0
+    for idx in order:
+        grp = [groups_all[idx]]
+        t0 = time.perf_counter()
+        OA.backward(p, Q, K, V, O_np, dO, LSE_np, mask, groups=grp)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    return per_group * done / t_total / 1e12, done, len(groups_all), t_total
+
+
+# --------------------------------------------------------------- main arms
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    make, seed, desc = WORKLOADS[args.workload]
+    p = make()
+    from oracle import attention as OA
+    Qn, Kn, Vn, dOn, maskn = W.make_inputs(p, seed)
+    f = lambda x: x.astype(np.float64)  # noqa: E731
+    groups_all = [(b, g) for b in range(p.batch) for g in range(p.num_kv_heads)]
+    per_group = MET.counted_flops(p) / len(groups_all)
+    vals = []
+    rng = np.random.default_rng(0)
+    for step in range(args.warmup + args.steps):
+        grp = [groups_all[int(rng.integers(len(groups_all)))]]
+        O, LSE = OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)  # untimed inputs
+        t0 = time.perf_counter()
+        OA.backward(p, f(Qn), f(Kn), f(Vn), O, f(dOn), LSE, maskn, groups=grp)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            vals.append(per_group / dt / 1e12)
+    value = statistics.mean(vals)
+    cores = os.cpu_count()
+    sample = f"one (batch, kv-head) group of {len(groups_all)} per step, fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_group / (value * 1e12) * 1e3 * len(groups_all),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": desc, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import attention_backward_pass_gb300 as ab
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    ab.load_library()
+    make, seed, desc = WORKLOADS[args.workload]
+    p = make()
+    x = device_inputs(p, seed, device)
+    tdt = x["Q"].dtype
+    dQ = torch.empty(p.q_shape(), dtype=tdt, device=device)
+    dK = torch.empty(p.kv_shape(), dtype=tdt, device=device)
+    dV = torch.empty(p.kv_shape(), dtype=tdt, device=device)
+    ws = ab.alloc_workspace(p, device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ab.attn_bwd(p, x["Q"], x["K"], x["V"], x["O"], x["dO"], x["LSE"], x["mask"], dQ, dK, dV,
+                    ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        e = evs[k]
+        e[0].record(stream)
+        ab.attn_bwd_prepare(p, x["Q"], x["K"], x["O"], x["dO"], x["LSE"], dQ, ws)
+        e[1].record(stream)
+        ab.attn_bwd_tiles(p, x["Q"], x["K"], x["V"], x["dO"], x["mask"], dQ, dK, dV, ws)
+        e[2].record(stream)
+        ab.attn_bwd_finish(p, dQ, ws)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    tile_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = MET.counted_flops(p)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # roofline of the dominant kernel (the fused tile kernel)
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    if p.dtype == W.DTYPE_BF16:
+        peak, peak_note = bf16_peak, f"bf16 dense, {peak_src} burst"
+    else:
+        peak = bf16_peak * TF32_OVER_BF16
+        peak_note = f"tf32 dense = {peak_src} bf16 burst x nominal 1.1/2.25"
+    tile_mean = statistics.mean(tile_ms)
+    achieved = flops / (tile_mean * 1e-3) / 1e12
+    traffic = read_traffic(args.workload)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(p, x, dQ, dK, dV, ws, args, stream, world)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        O_np = x["O"].float().cpu().numpy().astype(np.float64)
+        LSE_np = x["LSE"].cpu().numpy().astype(np.float64)
+        val, done, tot, secs = oracle_sample_tflops(p, x["numpy"], O_np, LSE_np, budget_s=12.0)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{done} of {tot} (batch, kv-head) groups, {secs:.1f} s, fp64 numpy"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if p.dtype == W.DTYPE_BF16 else "tf32",
+            "data": "synthetic",
+            "config": {"workload": desc, "l2": "flushed between timed steps (256 MiB write)",
+                       "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "dkdv_kernel (tcgen05 tile kernel)", "peak_source": peak_note,
+                         "kernel_ms": tile_mean, "prep_ms": statistics.mean(prep_ms)},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": ab.kernels_per_call(p) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
+    import torch
+    import attention_backward_pass_gb300 as ab
+    names = ["Q", "K", "V", "O", "dO", "LSE"] + (["mask"] if x["mask"] is not None else [])
+    host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in names}
+    for k in names:
+        host[k].copy_(x[k])
+    dev = {k: torch.empty_like(x[k]) for k in names}
+    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (dQ, dK, dV)]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    n = max(3, min(args.steps, 10))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n + 2)]
+    for i in range(n + 2):  # first two untimed (warm-up)
+        evs[i][0].record(stream)
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        ab.attn_bwd(p, dev["Q"], dev["K"], dev["V"], dev["O"], dev["dO"], dev["LSE"],
+                    dev.get("mask"), dQ, dK, dV, ws)
+        for t_h, t_d in zip(outs_h, (dQ, dK, dV)):
+            t_h.copy_(t_d, non_blocking=True)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs[2:]) / n
+    if world > 1:
+        t = torch.tensor([ms], device=dQ.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = MET.counted_flops(p) * world / (ms * 1e-3) / 1e12
+    return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def read_traffic(workload):
+    """DRAM bytes per launch of the tile kernel from the committed ncu summary
+    (profiles/dkdv_<workload>.md, line 'traffic_bytes_per_launch: N'), or None."""
+    path = os.path.join(ROOT, "profiles", f"dkdv_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            if line.strip().startswith("traffic_bytes_per_launch:"):
+                try:
+                    return float(line.split(":", 1)[1].split()[0])
+                except ValueError:
+                    return None
+    return None
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

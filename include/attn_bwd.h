@@ -125,6 +125,28 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
                      void* stream);
 
 /*
+ * attn_bwd as three stages, for callers that want to schedule or time them
+ * separately (attn_bwd == prepare, tiles, finish on one stream; same
+ * arguments and rules as attn_bwd):
+ *  attn_bwd_prepare  per-row Delta_i = dO_i . O_i (the Metal page's
+ *                    "D = rowsum(dO * O)") and LSE * log2(e) into the
+ *                    workspace, zeroes the fp32 dQ accumulator, and for fp32
+ *                    writes the TF32-rounded transposed copies Q^T, dO^T, K^T
+ *                    the tensor-core products read.
+ *  attn_bwd_tiles    the fused tile kernel: recomputes P, forms dS and
+ *                    produces dK, dV and the dQ accumulation.
+ *  attn_bwd_finish   bf16 only: converts the fp32 dQ accumulator to dQ.
+ */
+attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
+                             const void* O, const void* dO, const float* LSE, void* dQ,
+                             void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                           const void* dO, const float* mask, void* dQ, void* dK, void* dV,
+                           void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Decode (one query per head) backward, pass 1 of the decode page
  * ("rullama attention_backward_dq.wgsl"): probabilities are given and the
  * scores were unscaled, kv = h / (n_heads / n_kv_heads):
