@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libattnbwd.so")
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
-                -3: "CUDA error", -4: "device wait timed out", -5: "workspace problem"}
+                -3: "CUDA error", -4: "device wait timed out", -5: "workspace problem",
+                -6: "problem exceeds the fixed no-allocation scratch array"}
 ATTN_F32, ATTN_BF16 = 0, 1
 ATTN_LAYOUT_BHSD, ATTN_LAYOUT_BSHD = 0, 1
 
@@ -67,6 +68,8 @@ _SIGS = {
     "attn_bwd_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdDecodeParams)]),
     "attn_bwd_decode": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P, _P, _P,
                                        _P, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P,
+                                               _P, _P, _P, _P]),
     "attn_dropout_keep_mask": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), ctypes.c_int32,
                                               ctypes.c_int32, _P, _P]),
     "attn_bwd_query_range": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), ctypes.c_int32,
@@ -212,6 +215,15 @@ def attn_bwd_decode(p, k_hist, v_hist, probs, d_out, d_scores, d_q, workspace, s
                              ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                              _stream_ptr(stream))
     _check("attn_bwd_decode", st)
+
+
+def attn_bwd_decode_noalloc(p, k_hist, v_hist, probs, d_out, d_scores, d_q, stream=None):
+    """Decode backward with the library's fixed scratch array instead of a
+    workspace, for callers that cannot allocate device memory."""
+    st = load_library().attn_bwd_decode_noalloc(ctypes.byref(make_decode_params(p)), _ptr(k_hist),
+                                                _ptr(v_hist), _ptr(probs), _ptr(d_out),
+                                                _ptr(d_scores), _ptr(d_q), _stream_ptr(stream))
+    _check("attn_bwd_decode_noalloc", st)
 
 
 def dropout_keep_mask(p, b, h, keep, stream=None):

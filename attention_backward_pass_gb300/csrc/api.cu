@@ -169,6 +169,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
     case ATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case ATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed no-allocation scratch array";
   }
   return "unknown status";
 }

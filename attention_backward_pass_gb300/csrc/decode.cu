@@ -351,3 +351,65 @@ cudaError_t launch_decode(const attn_bwd_decode_params& p, const float* k_hist,
 }
 
 }  // namespace attnbwd
+
+// ------------------------------------------------------------------------
+// Decode backward without a caller-supplied workspace.
+//
+// The per-split partial sums live in a fixed device array compiled into the
+// library instead of caller memory.  Every GPU that loads the library holds
+// this array until the process exits.  Its device address is looked up once
+// per device (on the first call made with that device current).
+// ------------------------------------------------------------------------
+#include <mutex>
+
+namespace attnbwd {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = ATTN_DECODE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {nullptr};
+
+// Device address of the scratch array for the current device (nullptr on error).
+float* noalloc_scratch_for_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    float* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return nullptr;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace attnbwd
+
+extern "C" attn_status attn_bwd_decode_noalloc(const attn_bwd_decode_params* p,
+                                               const float* k_hist, const float* v_hist,
+                                               const float* probs, const float* d_out,
+                                               float* d_scores, float* d_q, void* stream) {
+  using namespace attnbwd;
+  // argument checks of attn_bwd_decode (0 means the problem is invalid)
+  if (attn_bwd_decode_workspace_size(p) == 0) return ATTN_ERR_INVALID;
+  const void* ptrs[] = {k_hist, v_hist, probs, d_out, d_scores, d_q};
+  for (const void* q : ptrs)
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u)) return ATTN_ERR_INVALID;
+  // as many history splits as the fixed array can hold, at most the usual number
+  int n_split = decode_num_splits(*p);
+  while (n_split > 1 && decode_partials_floats(*p, n_split) * sizeof(float) > kNoAllocScratchBytes)
+    --n_split;
+  if (decode_partials_floats(*p, n_split) * sizeof(float) > kNoAllocScratchBytes)
+    return ATTN_ERR_SCRATCH_LIMIT;
+  float* scratch = noalloc_scratch_for_current_device();
+  if (!scratch) return ATTN_ERR_CUDA;
+  // every split's slot is fully rewritten by the kernel: nothing to clear
+  if (launch_decode(*p, k_hist, v_hist, probs, d_out, d_scores, d_q, scratch, n_split,
+                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}

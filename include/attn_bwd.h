@@ -43,7 +43,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. head_dim 96) */
   ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   ATTN_ERR_TIMEOUT = -4,     /* a kernel's bounded wait ran out (device error word) */
-  ATTN_ERR_WORKSPACE = -5    /* workspace missing, too small or misaligned */
+  ATTN_ERR_WORKSPACE = -5,   /* workspace missing, too small or misaligned */
+  ATTN_ERR_SCRATCH_LIMIT = -6 /* problem needs more than the library's fixed scratch array */
 } attn_status;
 
 typedef enum {
@@ -176,6 +177,38 @@ attn_status attn_bwd_decode(const attn_bwd_decode_params* p, const float* k_hist
                             const float* v_hist, const float* probs, const float* d_out,
                             float* d_scores, float* d_q, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point.  Some callers cannot give the
+ * library a workspace: code that runs where no allocator is available or
+ * allowed -- a plugin interface that only passes input and output tensors, a
+ * process whose device memory is planned up front and may not grow, a
+ * real-time path where cudaMalloc's implicit synchronisation and failure modes
+ * are not acceptable.  This variant takes the same inputs and outputs as
+ * attn_bwd_decode but no workspace; it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Scratch: the partial sums go to one fixed array of
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory inside the
+ * library; every GPU that loads the library keeps that array until the
+ * process exits.  The array must hold, for at least one history split,
+ * num_seqs * n_heads * (1 + 2 * head_dim) floats (e.g. 64 sequences x 8 heads
+ * x head_dim 256 take 1 MiB per split); larger problems are rejected with
+ * ATTN_ERR_SCRATCH_LIMIT.  When the usual number of splits does not fit,
+ * fewer are used, so results can differ from attn_bwd_decode in the last bits.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current): make that first call before capturing
+ * the stream into a CUDA graph.  All calls share the one array and nothing in
+ * it is cleared between calls (each call rewrites every value it reads), so
+ * calls that can overlap on the GPU -- on different streams or from different
+ * host threads -- race; the caller must order them.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status attn_bwd_decode_noalloc(const attn_bwd_decode_params* p, const float* k_hist,
+                                    const float* v_hist, const float* probs, const float* d_out,
+                                    float* d_scores, float* d_q, void* stream);
 
 /*
  * Writes the dropout keep mask of slice (b, h) as bytes keep[i * seq_k + j]
