@@ -20,19 +20,27 @@
 //    as an MN-major operand (rows = K).
 //  * fp32 (TF32 products): the tensor cores take TF32 operands K-major only,
 //    so the contractions over queries (GEMM3/4) and keys (GEMM5) read
-//    transposed copies Q^T, dO^T, K^T that the transpose pre-pass writes to
-//    the workspace, and the softmax group also writes dS' in [query][key]
-//    orientation.
+//    transposed copies Q^T, dO^T, K^T that the prepare stage writes to the
+//    workspace, and the softmax warps also write dS' in [query][key]
+//    orientation.  The natural tiles (GEMM1/2) and the transposed tiles
+//    (GEMM3/4) travel in separate rings, so a natural stage is released as
+//    soon as GEMM1/2 are done with it.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: K/V (and K^T) once, then per query tile Q, dO
-//               (and Q^T, dO^T), LSE2 and Delta into a ring of ST stages
-//   warp 1      MMA issuer (one elected lane)
-//   warp 2      TMEM allocator
-//   warps 4-7   softmax group: one key row per TMEM lane; turns S^T and dP^T
-//               into P o M and dS' and stores them to shared memory as MMA
-//               operands; at the end writes dK and dV
-//   warps 8-11  dQ group: drains the GEMM5 accumulator into global memory
+// Pipeline.  GEMM1/2 of tile t are issued as soon as the softmax warps have
+// read tile t-NSB's scores out of tensor memory (NSB = 1 or 2 score
+// buffers), GEMM3-5 of tile t-1 right after; the softmax warps compute tile t
+// while the tensor cores finish tile t-1 and start tile t+1, and only wait
+// for GEMM3-5 of t-1 before overwriting the shared P / dS' tiles.
+//
+// Warp roles (512 threads):
+//   warp 0       TMA producer
+//   warp 1       MMA issuer (one elected lane)
+//   warp 2       TMEM allocator
+//   warps 4-11   softmax: warp w serves TMEM sub-partition w % 4 (its key
+//                rows) and half (w - 4) / 4 of the query columns; turns S^T
+//                and dP^T into P o M and dS', stores them as MMA operands, and
+//                at the end writes dK and dV
+//   warps 12-15  dQ: drain the GEMM5 accumulator into global memory
 // Accumulators with M = 64 rows live in lanes 0-15 of each 32-lane TMEM
 // sub-partition (row r -> lane (r / 16) * 32 + r % 16); M = 128 rows map
 // one-to-one.  Every tcgen05.ld is executed by whole warps.
@@ -51,29 +59,29 @@ template <bool BF16, int D>
 struct Cfg;
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
-  static constexpr int BN = 128, BM = 32, ST = 2;
+  static constexpr int BN = 128, BM = 32, NAT = 3, TR = 2, NSB = 2;
   static constexpr bool KMAJ = true, DQT = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
-  static constexpr int BN = 64, BM = 32, ST = 1;
+  static constexpr int BN = 64, BM = 32, NAT = 2, TR = 1, NSB = 2;
   static constexpr bool KMAJ = true, DQT = true;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
-  static constexpr int BN = 128, BM = 128, ST = 2;
+  static constexpr int BN = 128, BM = 128, NAT = 2, TR = 0, NSB = 1;
   static constexpr bool KMAJ = false, DQT = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
-  static constexpr int BN = 128, BM = 64, ST = 3;
+  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1;
   static constexpr bool KMAJ = false, DQT = true;
 };
 
 template <bool BF16, int D>
 struct Layout {
   using C = Cfg<BF16, D>;
-  static constexpr int BM = C::BM, ST = C::ST, BN = C::BN;
+  static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB;
   static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT;
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
   static constexpr int W = 128 / E;       // elements per 128-byte segment
@@ -86,39 +94,45 @@ struct Layout {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + K_BYTES;  // must follow K (padded GEMM5 reads it)
   static constexpr int OFF_KT = OFF_V + K_BYTES;
-  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);
-  static constexpr int OFF_DO = OFF_Q + ST * Q_BYTES;
-  static constexpr int OFF_QT = OFF_DO + ST * Q_BYTES;
-  static constexpr int OFF_DOT = OFF_QT + (KMAJ ? ST * Q_BYTES : 0);
-  static constexpr int OFF_P = OFF_DOT + (KMAJ ? ST * Q_BYTES : 0);
+  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);  // natural ring [NAT]
+  static constexpr int OFF_DO = OFF_Q + NAT * Q_BYTES;
+  static constexpr int OFF_QT = OFF_DO + NAT * Q_BYTES;        // transposed ring [TR]
+  static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
+  static constexpr int OFF_P = OFF_DOT + TR * Q_BYTES;
   static constexpr int OFF_DS = OFF_P + P_BYTES;
   static constexpr int OFF_DSN = OFF_DS + P_BYTES;
+  static constexpr int ROW_ST = KMAJ ? TR : NAT;  // ring that carries LSE2 / Delta
   static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? P_BYTES : 0);
-  static constexpr int OFF_DELTA = OFF_LSE + ST * BM * 4;
-  static constexpr int OFF_BAR = OFF_DELTA + ST * BM * 4;
-  static constexpr int NUM_BARS = 2 * ST + 7;
+  static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
+  static constexpr int OFF_BAR = OFF_DELTA + ROW_ST * BM * 4;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * NSB + 7;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
-  static constexpr int STAGE_TX = (KMAJ ? 4 : 2) * Q_BYTES + 2 * BM * 4;
+  static constexpr int NAT_TX = 2 * Q_BYTES + (KMAJ ? 0 : 2 * BM * 4);
+  static constexpr int TR_TX = 2 * Q_BYTES + 2 * BM * 4;
   static constexpr int KV_TX = (KMAJ ? 3 : 2) * K_BYTES;
   // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
   static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
   static constexpr int N5 = DQT ? BM : D;
-  // tensor memory columns
-  static constexpr int T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + D,
-                       T_DQ = 2 * BM + 2 * D;
+  // tensor memory columns: NSB x (S^T, dP^T), then dV, dK, dQ
+  static constexpr int T_DV = 2 * BM * NSB, T_DK = T_DV + D, T_DQ = T_DK + D;
   static constexpr int T_USED = T_DQ + N5;
   static constexpr int T_ALLOC = T_USED <= 256 ? 256 : 512;
-  static_assert(T_USED <= 512, "tensor memory budget");
+  // softmax split: two warps per TMEM sub-partition, each on half the columns
+  static constexpr int COLS = BM / 2;
+  static_assert(T_USED <= 512 && TR_TX > 0, "tensor memory budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(BM % 32 == 0 && (BM % W == 0 || BM < W), "query tile");
-  static_assert(!KMAJ || BM % W == 0, "transposed tiles are whole 128-byte blocks");
+  static_assert(COLS % 16 == 0, "softmax column chunks");
+  static_assert(!KMAJ || (BM % W == 0 && TR >= 1), "transposed tiles are whole blocks");
+  static_assert(KMAJ || NAT >= 2, "stages are released only after GEMM3/4");
   static_assert(BN == 64 || BN == 128, "key tile");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kDqThreads = 128;
 
 __device__ __forceinline__ uint32_t sw_off(int blk, int rows, int row, int pos_bytes) {
   return (uint32_t)(blk * rows * 128 + row * 128 + ((((pos_bytes >> 4) ^ (row & 7))) << 4) +
@@ -173,6 +187,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Warp-uniform bounded wait: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+  return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, err));
+}
+
 struct TileWork {
   int b, kvh, k0, q_begin, q_end, q_first, tiles_per_head, total;
 };
@@ -193,6 +212,21 @@ __device__ __forceinline__ TileWork tile_work(const TileArgs& a) {
   return w;
 }
 
+// True when every (query, key) pair of the tile is in range and visible and
+// no mask or dropout applies, so P needs no per-pair test.
+__device__ __forceinline__ bool tile_is_plain(const TileArgs& a, int q0, int BM, int k0, int BN) {
+  if (a.has_mask || a.dropout) return false;
+  if (q0 + BM > a.Sq || k0 + BN > a.Sk) return false;
+  const long long qa_min = (long long)q0 + a.causal_offset, qa_max = qa_min + BM - 1;
+  const long long k_min = k0, k_max = (long long)k0 + BN - 1;
+  if (a.causal && k_max > qa_min) return false;
+  if (a.window > 0) {
+    const long long far = max(qa_max - k_min, k_max - qa_min);
+    if (far >= a.window) return false;
+  }
+  return true;
+}
+
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -201,21 +235,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_kt,
                 const __grid_constant__ CUtensorMap tm_dot, const TileArgs a) {
   using L = Layout<BF16, D>;
-  constexpr int BM = L::BM, ST = L::ST, BN = L::BN, W = L::W, E = L::E;
+  constexpr int BM = L::BM, NAT = L::NAT, TR = L::TR, NSB = L::NSB, BN = L::BN, W = L::W,
+                E = L::E;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* full = bars;              // [ST] stage loaded (TMA tx)
-  uint64_t* empty = bars + ST;        // [ST] stage consumed (MMA commit)
-  uint64_t* kv_full = bars + 2 * ST;  // resident key tiles loaded
-  uint64_t* s_full = kv_full + 1;     // GEMM1/2 done
-  uint64_t* p_full = kv_full + 2;     // P / dS' in smem (128 arrivals)
-  uint64_t* mma5_done = kv_full + 3;  // GEMM3/4/5 done
-  uint64_t* dq_free = kv_full + 4;    // dQ accumulator drained (128 arrivals)
-  uint64_t* acc_done = kv_full + 5;   // all products done
-  uint64_t* final_bar = kv_full + 6;  // unwinding: products in flight done
+  uint64_t* nat_full = bars;                 // [NAT] natural tiles landed (TMA tx)
+  uint64_t* nat_empty = nat_full + NAT;      // [NAT] natural stage free (MMA commit)
+  uint64_t* tr_full = nat_empty + NAT;       // [TR] transposed tiles + LSE2/Delta landed
+  uint64_t* tr_empty = tr_full + TR;         // [TR] transposed stage free (MMA commit)
+  uint64_t* s_full = tr_empty + TR;          // [NSB] GEMM1/2 done into score buffer b
+  uint64_t* s_free = s_full + NSB;           // [NSB] softmax warps have read buffer b
+  uint64_t* kv_full = s_free + NSB;          // resident key tiles landed
+  uint64_t* p_full = kv_full + 1;            // P / dS' in shared memory
+  uint64_t* mma5_done = kv_full + 2;         // GEMM3/4/5 done
+  uint64_t* dq_free = kv_full + 3;           // dQ accumulator drained
+  uint64_t* acc_done = kv_full + 4;          // all products done
+  uint64_t* final_bar = kv_full + 5;         // unwinding: products in flight done
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
+  // the ring whose stage carries LSE2 / Delta of a tile, and its depth
+  uint64_t* row_full = L::KMAJ ? tr_full : nat_full;
+  constexpr int RST = L::ROW_ST;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -223,15 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = w.total;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < NAT; ++s) {
+      mbar_init(&nat_full[s], 1);
+      mbar_init(&nat_empty[s], 1);
+    }
+    for (int s = 0; s < TR; ++s) {
+      mbar_init(&tr_full[s], 1);
+      mbar_init(&tr_empty[s], 1);
+    }
+    for (int s = 0; s < NSB; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], kSoftmaxThreads);
     }
     mbar_init(kv_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, kSoftmaxThreads);
     mbar_init(mma5_done, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, kDqThreads);
     mbar_init(acc_done, 1);
     mbar_init(final_bar, 1);
     fence_barrier_init();
@@ -264,38 +312,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + L::OFF_KT + cb * D * 128, &tm_kt, kv_full, w.k0 + cb * W, 0, bhkv,
                       0);
       }
-      int issued = 0;
+      int nat_issued = 0, tr_issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % ST;
-        if (t >= ST && !mbar_wait(&empty[s], ((t / ST) - 1) & 1, a.err)) break;
         const int g = t / w.tiles_per_head;
         const int h = w.kvh * a.group + g;
+        const int bh = w.b * a.H + h;
         const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-        mbar_expect_tx(&full[s], L::STAGE_TX);
+        const long long row = (long long)bh * a.sq_pad + q0;
+        // natural Q / dO tiles (and, for bf16, LSE2 / Delta)
+        const int s = t % NAT;
+        if (t >= NAT && !mbar_wait(&nat_empty[s], ((t / NAT) - 1) & 1, a.err)) break;
+        mbar_expect_tx(&nat_full[s], L::NAT_TX);
         for (int cb = 0; cb < L::NB_D; ++cb) {
-          tma_load_4d(smem + L::OFF_Q + s * L::Q_BYTES + cb * BM * 128, &tm_q, &full[s], cb * W,
-                      q0, h, w.b);
-          tma_load_4d(smem + L::OFF_DO + s * L::Q_BYTES + cb * BM * 128, &tm_do, &full[s],
+          tma_load_4d(smem + L::OFF_Q + s * L::Q_BYTES + cb * BM * 128, &tm_q, &nat_full[s],
+                      cb * W, q0, h, w.b);
+          tma_load_4d(smem + L::OFF_DO + s * L::Q_BYTES + cb * BM * 128, &tm_do, &nat_full[s],
                       cb * W, q0, h, w.b);
         }
+        if constexpr (!L::KMAJ) {
+          bulk_load(smem + L::OFF_LSE + s * BM * 4, a.lse2 + row, BM * 4, &nat_full[s]);
+          bulk_load(smem + L::OFF_DELTA + s * BM * 4, a.delta + row, BM * 4, &nat_full[s]);
+        }
+        nat_issued = t + 1;
         if constexpr (L::KMAJ) {
-          const int bh = w.b * a.H + h;
+          // transposed Q^T / dO^T tiles [D rows][BM] and LSE2 / Delta
+          const int r = t % TR;
+          if (t >= TR && !mbar_wait(&tr_empty[r], ((t / TR) - 1) & 1, a.err)) break;
+          mbar_expect_tx(&tr_full[r], L::TR_TX);
           for (int cb = 0; cb < BM / W; ++cb) {
-            tma_load_4d(smem + L::OFF_QT + s * L::Q_BYTES + cb * D * 128, &tm_qt, &full[s],
+            tma_load_4d(smem + L::OFF_QT + r * L::Q_BYTES + cb * D * 128, &tm_qt, &tr_full[r],
                         q0 + cb * W, 0, bh, 0);
-            tma_load_4d(smem + L::OFF_DOT + s * L::Q_BYTES + cb * D * 128, &tm_dot, &full[s],
+            tma_load_4d(smem + L::OFF_DOT + r * L::Q_BYTES + cb * D * 128, &tm_dot, &tr_full[r],
                         q0 + cb * W, 0, bh, 0);
           }
+          bulk_load(smem + L::OFF_LSE + r * BM * 4, a.lse2 + row, BM * 4, &tr_full[r]);
+          bulk_load(smem + L::OFF_DELTA + r * BM * 4, a.delta + row, BM * 4, &tr_full[r]);
+          tr_issued = t + 1;
         }
-        const long long row = (long long)(w.b * a.H + h) * a.sq_pad + q0;
-        bulk_load(smem + L::OFF_LSE + s * BM * 4, a.lse2 + row, BM * 4, &full[s]);
-        bulk_load(smem + L::OFF_DELTA + s * BM * 4, a.delta + row, BM * 4, &full[s]);
-        issued = t + 1;
       }
       // let every copy still in flight land before the CTA can exit
       drain_wait(kv_full, 0);
-      for (int t = (issued > ST ? issued - ST : 0); t < issued; ++t)
-        drain_wait(&full[t % ST], (t / ST) & 1);
+      for (int t = (nat_issued > NAT ? nat_issued - NAT : 0); t < nat_issued; ++t)
+        drain_wait(&nat_full[t % NAT], (t / NAT) & 1);
+      if constexpr (L::KMAJ) {
+        for (int t = (tr_issued > TR ? tr_issued - TR : 0); t < tr_issued; ++t)
+          drain_wait(&tr_full[t % TR], (t / TR) & 1);
+      }
     }
     __syncwarp();  // reconverge before the block-wide barrier at the end
   } else if (warp == 1) {
@@ -309,24 +371,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, !L::KMAJ);
       constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, !L::KMAJ, !L::KMAJ);
       bool ok = mbar_wait(kv_full, 0, a.err);
-      auto issue_front = [&](int t) {  // GEMM1, GEMM2 of tile t
-        const int s = t % ST;
+      auto issue_front = [&](int t) -> bool {  // GEMM1, GEMM2 of tile t
+        const int s = t % NAT, b = t % NSB;
+        if (!mbar_wait(&nat_full[s], (t / NAT) & 1, a.err)) return false;
+        if (t >= NSB && !mbar_wait(&s_free[b], ((t / NSB) - 1) & 1, a.err)) return false;
+        tc_fence_after();
         const uint32_t sQ = smem_u32(smem + L::OFF_Q + s * L::Q_BYTES);
         const uint32_t sDO = smem_u32(smem + L::OFF_DO + s * L::Q_BYTES);
+        const uint32_t t_s = tmem + b * 2 * BM, t_dp = t_s + BM;
 #pragma unroll
         for (int ks = 0; ks < D / L::KSTEP; ++ks) {
           const int kb = ks * 32;
           const uint32_t ka = (kb / 128) * BN * 128 + (kb % 128);
           const uint32_t qa = (kb / 128) * BM * 128 + (kb % 128);
-          mma_ss<BF16>(tmem + L::T_S, sw128_desc(sK + ka, 16, 1024), sw128_desc(sQ + qa, 16, 1024),
-                       id_s, ks > 0);
-          mma_ss<BF16>(tmem + L::T_DP, sw128_desc(sV + ka, 16, 1024),
-                       sw128_desc(sDO + qa, 16, 1024), id_s, ks > 0);
+          mma_ss<BF16>(t_s, sw128_desc(sK + ka, 16, 1024), sw128_desc(sQ + qa, 16, 1024), id_s,
+                       ks > 0);
+          mma_ss<BF16>(t_dp, sw128_desc(sV + ka, 16, 1024), sw128_desc(sDO + qa, 16, 1024), id_s,
+                       ks > 0);
         }
-        mma_commit(s_full);
+        mma_commit(&s_full[b]);
+        if constexpr (L::KMAJ) mma_commit(&nat_empty[s]);  // natural tiles done with
+        return true;
       };
       auto issue_back = [&](int t) -> bool {  // GEMM3, GEMM4, GEMM5 of tile t
-        const int s = t % ST;
+        if (!mbar_wait(p_full, t & 1, a.err)) return false;
+        const int s = t % NAT, r = L::KMAJ ? t % TR : 0;
+        if constexpr (L::KMAJ) {
+          if (!mbar_wait(&tr_full[r], (t / TR) & 1, a.err)) return false;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
           const int kb = ks * 32;
@@ -335,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint64_t bdo, bq;
           if constexpr (L::KMAJ) {  // transposed tiles [D rows][BM], K-major
             const uint32_t ta = (kb / 128) * D * 128 + (kb % 128);
-            bdo = sw128_desc(smem_u32(smem + L::OFF_DOT + s * L::Q_BYTES) + ta, 16, 1024);
-            bq = sw128_desc(smem_u32(smem + L::OFF_QT + s * L::Q_BYTES) + ta, 16, 1024);
+            bdo = sw128_desc(smem_u32(smem + L::OFF_DOT + r * L::Q_BYTES) + ta, 16, 1024);
+            bq = sw128_desc(smem_u32(smem + L::OFF_QT + r * L::Q_BYTES) + ta, 16, 1024);
           } else {  // natural tiles [BM rows][D] read MN-major
             const uint32_t ra = ks * L::KSTEP * 128;
             bdo = sw128_desc(smem_u32(smem + L::OFF_DO + s * L::Q_BYTES) + ra, BM * 128, 1024);
@@ -366,104 +439,118 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(mma5_done);
-        mma_commit(&empty[s]);
+        if constexpr (L::KMAJ) {
+          mma_commit(&tr_empty[r]);
+        } else {
+          mma_commit(&nat_empty[s]);
+        }
         return true;
       };
-      // With two or more stages GEMM1/2 of tile t are issued before GEMM3-5 of
-      // tile t-1, so the softmax group can start on tile t while the tensor
-      // cores finish t-1.  With one stage tile t's operands only arrive after
-      // GEMM3-5 of t-1 released the stage, so the order is back(t-1), front(t).
       for (int t = 0; ok && t < T; ++t) {
-        const int s = t % ST;
-        if (ST == 1 && t > 0) {
-          if (!mbar_wait(p_full, (t - 1) & 1, a.err)) { ok = false; break; }
-          tc_fence_after();
-          if (!issue_back(t - 1)) { ok = false; break; }
-        }
-        if (!mbar_wait(&full[s], (t / ST) & 1, a.err)) { ok = false; break; }
-        if (ST > 1 && t > 0 && !mbar_wait(p_full, (t - 1) & 1, a.err)) { ok = false; break; }
-        tc_fence_after();
-        issue_front(t);
-        if (ST > 1 && t > 0 && !issue_back(t - 1)) { ok = false; break; }
+        if (!issue_front(t)) { ok = false; break; }
+        if (t > 0 && !issue_back(t - 1)) { ok = false; break; }
       }
-      if (ok) {
-        if (mbar_wait(p_full, (T - 1) & 1, a.err)) {
-          tc_fence_after();
-          if (issue_back(T - 1)) mma_commit(acc_done);
-        }
-      }
+      if (ok && issue_back(T - 1)) mma_commit(acc_done);
       mma_commit(final_bar);
     }
     __syncwarp();  // reconverge before the block-wide barrier at the end
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ softmax group
-    const int j = acc_row<BN>((warp - 4) * 32 + lane);  // key row of this lane, or -1
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ softmax warps
+    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int j = acc_row<BN>(quad * 32 + lane);  // key row of this lane, or -1
     const int kj = w.k0 + (j >= 0 ? j : 0);
     const bool key_ok = j >= 0 && kj < a.Sk;
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint8_t* sP = smem + L::OFF_P;
     uint8_t* sdS = smem + L::OFF_DS;
     uint8_t* sdSN = smem + L::OFF_DSN;
+    const int cbeg = half * L::COLS;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int s = t % ST;
+      const int b = t % NSB, rs = t % RST;
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-      // warp-uniform decisions: the tcgen05 loads below need the whole warp
-      bool got = mbar_wait(s_full, t & 1, a.err);
-      if (got && t > 0) got = mbar_wait(mma5_done, (t - 1) & 1, a.err);
-      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      if (!warp_wait(&s_full[b], (t / NSB) & 1, a.err) ||
+          !warp_wait(&row_full[rs], (t / RST) & 1, a.err)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + s * BM * 4);
-      const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + s * BM * 4);
+      const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + rs * BM * 4);
+      const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + rs * BM * 4);
       const uint32_t bh = (uint32_t)(w.b * a.H + h);
+      const bool plain = tile_is_plain(a, q0, BM, w.k0, BN);
       const float* mrow = a.has_mask ? a.mask + w.b * a.msb + h * a.msh + (long long)kj * a.msk
                                      : nullptr;
+      const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BM; c0 += 16) {
-        uint32_t rs[16], rd[16];
-        tmem_ld16(tmem + lane_base + L::T_S + c0, rs);
-        tmem_ld16(tmem + lane_base + L::T_DP + c0, rd);
+      for (int c0 = cbeg; c0 < cbeg + L::COLS; c0 += 16) {
+        uint32_t rs16[16], rd16[16];
+        tmem_ld16(t_s + c0, rs16);
+        tmem_ld16(t_dp + c0, rd16);
         tmem_ld_wait();
-        if (j < 0) continue;  // lane holds no key row (M = 64 layout)
-        float pm[16], ds[16];
-        uint32_t words[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int q = q0 + c0 + c;
-          bool vis = (q < a.Sq) && key_ok;
-          const long long qa = (long long)q + a.causal_offset;
-          if (a.causal) vis = vis && ((long long)kj <= qa);
-          if (a.window > 0) {
-            const long long dist = qa >= kj ? qa - kj : kj - qa;
-            vis = vis && (dist < a.window);
-          }
-          float bias = 0.f;
-          if (a.has_mask && vis) {
-            const float m = __ldg(mrow + (long long)q * a.msq);
-            vis = m > -1.0e30f;
-            bias = m * kLog2e;
-          }
-          const float x = fmaf(__uint_as_float(rs[c]), a.scale_log2e, bias - sLSE[c0 + c]);
-          const float p = vis ? ex2_approx(x) : 0.f;
-          float mult = 1.f;
-          if (a.dropout) {
-            // one Philox call per 4 consecutive queries of this key
-            if ((c & 3) == 0) {
-              const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u, a.seed_lo,
-                                              a.seed_hi);
-              words[0] = r.w[0];
-              words[1] = r.w[1];
-              words[2] = r.w[2];
-              words[3] = r.w[3];
-            }
-            mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
-          }
-          const float dpv = __uint_as_float(rd[c]) * mult;
-          pm[c] = p * mult;
-          ds[c] = a.scale * p * (dpv - sDelta[c0 + c]);
+        if (c0 + 16 == cbeg + L::COLS) {  // this warp's last read of the score buffer
+          tc_fence_before();
+          mbar_arrive(&s_free[b]);
         }
+        float pm[16], ds[16];
+        if (j >= 0) {
+          if (plain) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(sLSE + c0 + c);
+              const float4 d4 = *reinterpret_cast<const float4*>(sDelta + c0 + c);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float p = ex2_approx(fmaf(__uint_as_float(rs16[c + u]), a.scale_log2e, -lv[u]));
+                pm[c + u] = p;
+                ds[c + u] = (p * a.scale) * (__uint_as_float(rd16[c + u]) - dv[u]);
+              }
+            }
+          } else {
+            uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int q = q0 + c0 + c;
+              bool vis = (q < a.Sq) && key_ok;
+              const int qa = q + (int)a.causal_offset;
+              if (a.causal) vis = vis && (kj <= qa);
+              if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
+              float bias = 0.f;
+              if (a.has_mask && vis) {
+                const float m = __ldg(mrow + (long long)q * a.msq);
+                vis = m > -1.0e30f;
+                bias = m * kLog2e;
+              }
+              const float x = fmaf(__uint_as_float(rs16[c]), a.scale_log2e, bias - sLSE[c0 + c]);
+              const float p = vis ? ex2_approx(x) : 0.f;
+              float mult = 1.f;
+              if (a.dropout) {
+                // one Philox call per 4 consecutive queries of this key
+                if ((c & 3) == 0) {
+                  const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u,
+                                                  a.seed_lo, a.seed_hi);
+                  words[0] = r.w[0];
+                  words[1] = r.w[1];
+                  words[2] = r.w[2];
+                  words[3] = r.w[3];
+                }
+                mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
+              }
+              pm[c] = p * mult;
+              ds[c] = (p * a.scale) * (__uint_as_float(rd16[c]) * mult - sDelta[c0 + c]);
+            }
+          }
+        }
+        // the previous tile's GEMM3-5 must be done with the shared P / dS' tiles
+        if (c0 == cbeg && t > 0 && !warp_wait(mma5_done, (t - 1) & 1, a.err)) {
+          ok = false;
+          break;
+        }
+        if (j < 0) continue;  // lane holds no key row (M = 64 layout)
         // 16 columns of row j into the swizzled P^T / dS'^T tiles [BN rows][BM]
         const int blk = c0 / W;
         const int pos = (c0 % W) * E;
@@ -481,38 +568,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
           }
         } else {
+          uint32_t dsr[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dsr[c] = to_tf32(ds[c]);
 #pragma unroll
           for (int h4 = 0; h4 < 4; ++h4) {
             const uint32_t off = sw_off(blk, BN, j, pos + h4 * 16);
             st_shared_v4(smem_u32(sP + off), to_tf32(pm[h4 * 4 + 0]), to_tf32(pm[h4 * 4 + 1]),
                          to_tf32(pm[h4 * 4 + 2]), to_tf32(pm[h4 * 4 + 3]));
-            st_shared_v4(smem_u32(sdS + off), to_tf32(ds[h4 * 4 + 0]), to_tf32(ds[h4 * 4 + 1]),
-                         to_tf32(ds[h4 * 4 + 2]), to_tf32(ds[h4 * 4 + 3]));
+            st_shared_v4(smem_u32(sdS + off), dsr[h4 * 4 + 0], dsr[h4 * 4 + 1], dsr[h4 * 4 + 2],
+                         dsr[h4 * 4 + 3]);
           }
           if constexpr (L::KMAJ) {
             // dS' also as [BM rows (queries)][BN keys] for GEMM5's K-major operand
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const uint32_t off = sw_off(j / W, BM, c0 + c, (j % W) * 4);
-              st_shared_b32(smem_u32(sdSN + off), to_tf32(ds[c]));
+              st_shared_b32(smem_u32(sdSN + off), dsr[c]);
             }
           }
         }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
-      tc_fence_before();
       mbar_arrive(p_full);
     }
     // --------------------------------------------------------- dK / dV epilogue
     bool have = ok && T > 0;
     if (have) {
-      have = !__any_sync(0xffffffffu, !mbar_wait(acc_done, 0, a.err));
+      have = warp_wait(acc_done, 0, a.err);
       tc_fence_after();
     }
     if (have || T == 0) {
       const long long off = row_offset(a.layout, w.b, w.kvh, key_ok ? kj : 0, a.Hkv, a.Sk, D);
+      constexpr int DH = D / 2;  // this warp's half of the head dimension
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = half * DH; c0 < (half + 1) * DH; c0 += 16) {
         uint32_t rv[16], rk[16];
         if (have) {  // whole warps: tcgen05.ld is warp-collective
           tmem_ld16(tmem + lane_base + L::T_DV + c0, rv);
@@ -549,15 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ group
-    const int r = acc_row<L::M5>((warp - 8) * 32 + lane);  // accumulator row, or -1
-    const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ warps
+    const int quad = warp & 3;
+    const int r = acc_row<L::M5>(quad * 32 + lane);  // accumulator row, or -1
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     for (int t = 0; t < T; ++t) {
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-      if (__any_sync(0xffffffffu, !mbar_wait(mma5_done, t & 1, a.err))) break;
+      if (!warp_wait(mma5_done, t & 1, a.err)) break;
       tc_fence_after();
       float v[L::N5];
 #pragma unroll

@@ -48,13 +48,15 @@ WORKLOADS = {
     "masked_dropout": (W.masked_dropout, 3,
                        "masked+dropout B2 H16 Sq512 Sk2048 D64 fp32 causal_offset1536 p0.1"),
     "tiny": (W.tiny, 0, "tiny B1 H2 S64 D64 fp32"),
+    "decode": (W.decode, 4, "decode backward: 64 seqs, 8 heads, 1 kv head, D256, history 4096, fp32"),
 }
+DECODE_METRIC = "decode attention-backward GB/s (d_scores+d_q) and % of HBM peak"
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal_mha", choices=sorted(WORKLOADS))
@@ -194,6 +196,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def load_under_clock_sampling(step, seconds=0.8):
+    """Untimed steps right before the timed ones, so that the clock sampler
+    (200 ms period) sees the GPU under this load; the timed region itself is
+    only milliseconds long."""
+    import torch
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+
 # --------------------------------------------------------------- CPU oracle
 
 def oracle_sample_tflops(p, numpy_inputs, O_np, LSE_np, budget_s: float, rng_seed=0):
@@ -296,6 +310,7 @@ def run_ours(args):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    load_under_clock_sampling(step)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -426,10 +441,100 @@ def read_traffic(workload):
     return None
 
 
+def run_decode(args):
+    """Decode backward: memory-bound; value = algorithmic bytes / time."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    ab.load_library()
+    make, seed, desc = WORKLOADS["decode"]
+    p = make()
+    k, v, d_out, logits = W.make_decode_inputs(p, seed)
+    lg = torch.from_numpy(logits).to(device)
+    probs = torch.softmax(lg, dim=-1).contiguous()  # input synthesis
+    t = {n: torch.from_numpy(a).to(device) for n, a in (("k", k), ("v", v), ("d_out", d_out))}
+    d_scores = torch.empty((p.num_seqs, p.n_heads, p.history_len), device=device)
+    d_q = torch.empty((p.num_seqs, p.n_heads, p.head_dim), device=device)
+    ws = ab.alloc_decode_workspace(p, device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ab.attn_bwd_decode(p, t["k"], t["v"], probs, t["d_out"], d_scores, d_q, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    load_under_clock_sampling(step)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:  # inputs (537 MB of K/V) are larger than L2
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set")
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total = sum(ms)
+    if world > 1:
+        tt = torch.tensor([total], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total = float(tt.item())
+    nbytes = MET.decode_bytes(p)
+    value = nbytes * world * args.steps / (total * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import decode as OD2
+        pr = probs.cpu().numpy()
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < 10.0 and n < p.num_seqs:
+            OD2.decode_backward(k, v, pr, d_out, seqs=[n])
+            n += 1
+        secs = time.perf_counter() - t0
+        cpu = {"value": nbytes / p.num_seqs * n / secs / 1e9, "unit": "GB/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n} of {p.num_seqs} sequences, {secs:.1f} s, fp64 numpy"}
+    if rank == 0:
+        mean_ms = statistics.mean(ms)
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": desc, "l2": "inputs larger than L2",
+                       "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": nbytes / (mean_ms * 1e-3) / 1e9,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": nbytes / (mean_ms * 1e-3) / 1e9 / peak, "traffic": None,
+                         "kernel": "decode_main_kernel + decode_finalize_kernel",
+                         "peak_source": f"{src} hbm_gbs"},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "decode":
+        return run_decode(args)
     return run_ours(args)
 
 
