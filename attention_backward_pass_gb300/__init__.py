@@ -77,8 +77,8 @@ _SIGS = {
                                             ctypes.POINTER(ctypes.c_int32)]),
     "attn_bwd_check_device_error": (ctypes.c_int, [ctypes.c_int32]),
     "attn_selftest_mma": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
-                                         _P, _P, _P]),
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, _P, _P, _P, _P, _P]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -248,8 +248,8 @@ def check_device_error(clear: bool = True) -> int:
     return int(load_library().attn_bwd_check_device_error(1 if clear else 0))
 
 
-def selftest_mma(dtype, M, N, K, a_mn, b_mn, A, B, C, dump=None, stream=None):
+def selftest_mma(dtype, M, N, K, a_mn, b_mn, A, B, C, dump=None, stream=None, a_tmem=False):
     lib = load_library()
-    st = lib.attn_selftest_mma(dtype, M, N, K, int(a_mn), int(b_mn), _ptr(A), _ptr(B), _ptr(C),
-                               _ptr(dump), _stream_ptr(stream))
+    st = lib.attn_selftest_mma(dtype, M, N, K, int(a_mn), int(b_mn), int(a_tmem), _ptr(A),
+                               _ptr(B), _ptr(C), _ptr(dump), _stream_ptr(stream))
     _check("attn_selftest_mma", st)

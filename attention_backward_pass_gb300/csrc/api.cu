@@ -411,10 +411,10 @@ attn_status attn_bwd_check_device_error(int32_t clear_it) {
 }
 
 attn_status attn_selftest_mma(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t a_mn,
-                              int32_t b_mn, const void* A, const void* B, float* C,
-                              float* tmem_dump, void* stream) {
+                              int32_t b_mn, int32_t a_tmem, const void* A, const void* B,
+                              float* C, float* tmem_dump, void* stream) {
   if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
-  return selftest_mma_launch(dtype, M, N, K, a_mn, b_mn, A, B, C, tmem_dump,
+  return selftest_mma_launch(dtype, M, N, K, a_mn, b_mn, a_tmem, A, B, C, tmem_dump,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 

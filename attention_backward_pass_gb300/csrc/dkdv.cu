@@ -59,29 +59,30 @@ template <bool BF16, int D>
 struct Cfg;
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
-  static constexpr int BN = 128, BM = 32, NAT = 3, TR = 2, NSB = 2;
+  static constexpr int BN = 128, BM = 32, NAT = 3, TR = 2, NSB = 2, PB = 2;
   static constexpr bool KMAJ = true, DQT = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
-  static constexpr int BN = 64, BM = 32, NAT = 2, TR = 1, NSB = 2;
+  static constexpr int BN = 64, BM = 32, NAT = 2, TR = 1, NSB = 2, PB = 1;
   static constexpr bool KMAJ = true, DQT = true;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
-  static constexpr int BN = 128, BM = 128, NAT = 2, TR = 0, NSB = 1;
+  static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1;
   static constexpr bool KMAJ = false, DQT = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
-  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1;
+  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1;
   static constexpr bool KMAJ = false, DQT = true;
 };
 
 template <bool BF16, int D>
 struct Layout {
   using C = Cfg<BF16, D>;
-  static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB;
+  static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB,
+                       PB = C::PB;
   static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT;
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
   static constexpr int W = 128 / E;       // elements per 128-byte segment
@@ -98,14 +99,17 @@ struct Layout {
   static constexpr int OFF_DO = OFF_Q + NAT * Q_BYTES;
   static constexpr int OFF_QT = OFF_DO + NAT * Q_BYTES;        // transposed ring [TR]
   static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
-  static constexpr int OFF_P = OFF_DOT + TR * Q_BYTES;
-  static constexpr int OFF_DS = OFF_P + P_BYTES;
-  static constexpr int OFF_DSN = OFF_DS + P_BYTES;
+  // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
+  static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
+  static constexpr int OFF_DSN = OFF_DS + (KMAJ ? 0 : P_BYTES);
   static constexpr int ROW_ST = KMAJ ? TR : NAT;  // ring that carries LSE2 / Delta
-  static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? P_BYTES : 0);
+  static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? PB * P_BYTES : 0);
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
-  static constexpr int OFF_BAR = OFF_DELTA + ROW_ST * BM * 4;
-  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * NSB + 7;
+  // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
+  static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
+  static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
+  static constexpr int OFF_BAR = OFF_STG + BM * STG_D * 4;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * NSB + 2 + PB + 6;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
@@ -115,8 +119,12 @@ struct Layout {
   // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
   static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
   static constexpr int N5 = DQT ? BM : D;
-  // tensor memory columns: NSB x (S^T, dP^T), then dV, dK, dQ
-  static constexpr int T_DV = 2 * BM * NSB, T_DK = T_DV + D, T_DQ = T_DK + D;
+  // tensor memory columns: NSB x (S^T, dP^T), PB x P^T (fp32: one column per
+  // element; bf16: two per column), fp32: PB x dS'^T, then dV, dK, dQ
+  static constexpr int PCOLS = BF16 ? BM / 2 : BM;
+  static constexpr int T_P = 2 * BM * NSB;
+  static constexpr int T_DS = T_P + PB * PCOLS;
+  static constexpr int T_DV = T_DS + (KMAJ ? PB * BM : 0), T_DK = T_DV + D, T_DQ = T_DK + D;
   static constexpr int T_USED = T_DQ + N5;
   static constexpr int T_ALLOC = T_USED <= 256 ? 256 : 512;
   // softmax split: two warps per TMEM sub-partition, each on half the columns
@@ -126,6 +134,7 @@ struct Layout {
   static_assert(COLS % 16 == 0, "softmax column chunks");
   static_assert(!KMAJ || (BM % W == 0 && TR >= 1), "transposed tiles are whole blocks");
   static_assert(KMAJ || NAT >= 2, "stages are released only after GEMM3/4");
+  static_assert(PB == 1 || PB == 2, "P / dS buffers");
   static_assert(BN == 64 || BN == 128, "key tile");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
@@ -192,6 +201,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
   return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, err));
 }
 
+// Named barrier 1 over the 128 dQ threads, combined with a vote: true only if
+// every participating thread passed `ok`.  All 128 threads always arrive, so
+// the group cannot split even when a wait gave up.
+__device__ __forceinline__ bool dq_group_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void dq_group_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 struct TileWork {
   int b, kvh, k0, q_begin, q_end, q_first, tiles_per_head, total;
 };
@@ -235,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_kt,
                 const __grid_constant__ CUtensorMap tm_dot, const TileArgs a) {
   using L = Layout<BF16, D>;
-  constexpr int BM = L::BM, NAT = L::NAT, TR = L::TR, NSB = L::NSB, BN = L::BN, W = L::W,
-                E = L::E;
+  constexpr int BM = L::BM, NAT = L::NAT, TR = L::TR, NSB = L::NSB, PB = L::PB, BN = L::BN,
+                W = L::W, E = L::E;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -247,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tr_empty = tr_full + TR;         // [TR] transposed stage free (MMA commit)
   uint64_t* s_full = tr_empty + TR;          // [NSB] GEMM1/2 done into score buffer b
   uint64_t* s_free = s_full + NSB;           // [NSB] softmax warps have read buffer b
-  uint64_t* kv_full = s_free + NSB;          // resident key tiles landed
-  uint64_t* p_full = kv_full + 1;            // P / dS' in shared memory
-  uint64_t* mma5_done = kv_full + 2;         // GEMM3/4/5 done
-  uint64_t* dq_free = kv_full + 3;           // dQ accumulator drained
-  uint64_t* acc_done = kv_full + 4;          // all products done
-  uint64_t* final_bar = kv_full + 5;         // unwinding: products in flight done
+  uint64_t* p_full = s_free + NSB;           // [2] P / dS' of a tile written (by parity)
+  uint64_t* mma5_par = p_full + 2;           // [PB] GEMM3/4/5 of a tile done (by t % PB)
+  uint64_t* kv_full = mma5_par + PB;         // resident key tiles landed
+  uint64_t* mma5_done = kv_full + 1;         // GEMM3/4/5 done (every tile, dQ warps)
+  uint64_t* dq_free = kv_full + 2;           // dQ accumulator drained
+  uint64_t* acc_done = kv_full + 3;          // all products done
+  uint64_t* final_bar = kv_full + 4;         // unwinding: products in flight done
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
   // the ring whose stage carries LSE2 / Delta of a tile, and its depth
   uint64_t* row_full = L::KMAJ ? tr_full : nat_full;
@@ -276,8 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], kSoftmaxThreads);
     }
+    mbar_init(&p_full[0], kSoftmaxThreads);
+    mbar_init(&p_full[1], kSoftmaxThreads);
+    for (int s = 0; s < PB; ++s) mbar_init(&mma5_par[s], 1);
     mbar_init(kv_full, 1);
-    mbar_init(p_full, kSoftmaxThreads);
     mbar_init(mma5_done, 1);
     mbar_init(dq_free, kDqThreads);
     mbar_init(acc_done, 1);
@@ -362,83 +394,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();  // reconverge before the block-wide barrier at the end
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Shared-memory descriptors are built once; every product then only adds
+    // a constant byte offset (>> 4) to the 14-bit start-address field.  Shared
+    // addresses stay below 256 KB, so the add never carries out of the field.
     if (elect_one_sync() && T > 0) {
-      const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
-      const uint32_t sKT = smem_u32(smem + L::OFF_KT);
-      const uint32_t sP = smem_u32(smem + L::OFF_P), sdS = smem_u32(smem + L::OFF_DS);
-      const uint32_t sdSN = smem_u32(smem + L::OFF_DSN);
       constexpr uint32_t id_s = make_idesc(BF16, BN, BM, false, false);
       constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, !L::KMAJ);
       constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, !L::KMAJ, !L::KMAJ);
+      // K-major tiles: LBO unused, SBO = 8 rows x 128 B
+      const uint64_t dK = sw128_desc(smem_u32(smem + L::OFF_K), 16, 1024);
+      const uint64_t dV = sw128_desc(smem_u32(smem + L::OFF_V), 16, 1024);
+      const uint64_t dS = sw128_desc(smem_u32(smem + L::OFF_DS), 16, 1024);
+      const uint64_t dKT = sw128_desc(smem_u32(smem + L::OFF_KT), 16, 1024);
+      const uint64_t dSN = sw128_desc(smem_u32(smem + L::OFF_DSN), 16, 1024);
+      const uint64_t dQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), 16, 1024);
+      const uint64_t dDO0 = sw128_desc(smem_u32(smem + L::OFF_DO), 16, 1024);
+      const uint64_t dQT0 = sw128_desc(smem_u32(smem + L::OFF_QT), 16, 1024);
+      const uint64_t dDOT0 = sw128_desc(smem_u32(smem + L::OFF_DOT), 16, 1024);
+      // MN-major views (bf16): LBO = bytes between 128-byte column blocks
+      const uint64_t mQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), BM * 128, 1024);
+      const uint64_t mDO0 = sw128_desc(smem_u32(smem + L::OFF_DO), BM * 128, 1024);
+      const uint64_t mK = sw128_desc(smem_u32(smem + L::OFF_K), BN * 128, 1024);
+      const uint64_t mS = sw128_desc(smem_u32(smem + L::OFF_DS), BN * 128, 1024);
+      auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
       bool ok = mbar_wait(kv_full, 0, a.err);
       auto issue_front = [&](int t) -> bool {  // GEMM1, GEMM2 of tile t
         const int s = t % NAT, b = t % NSB;
         if (!mbar_wait(&nat_full[s], (t / NAT) & 1, a.err)) return false;
         if (t >= NSB && !mbar_wait(&s_free[b], ((t / NSB) - 1) & 1, a.err)) return false;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(smem + L::OFF_Q + s * L::Q_BYTES);
-        const uint32_t sDO = smem_u32(smem + L::OFF_DO + s * L::Q_BYTES);
+        const uint64_t dQ = adv(dQ0, s * L::Q_BYTES), dDO = adv(dDO0, s * L::Q_BYTES);
         const uint32_t t_s = tmem + b * 2 * BM, t_dp = t_s + BM;
 #pragma unroll
         for (int ks = 0; ks < D / L::KSTEP; ++ks) {
-          const int kb = ks * 32;
+          const uint32_t kb = ks * 32;
           const uint32_t ka = (kb / 128) * BN * 128 + (kb % 128);
           const uint32_t qa = (kb / 128) * BM * 128 + (kb % 128);
-          mma_ss<BF16>(t_s, sw128_desc(sK + ka, 16, 1024), sw128_desc(sQ + qa, 16, 1024), id_s,
-                       ks > 0);
-          mma_ss<BF16>(t_dp, sw128_desc(sV + ka, 16, 1024), sw128_desc(sDO + qa, 16, 1024), id_s,
-                       ks > 0);
+          mma_ss<BF16>(t_s, adv(dK, ka), adv(dQ, qa), id_s, ks > 0);
+          mma_ss<BF16>(t_dp, adv(dV, ka), adv(dDO, qa), id_s, ks > 0);
         }
         mma_commit(&s_full[b]);
         if constexpr (L::KMAJ) mma_commit(&nat_empty[s]);  // natural tiles done with
         return true;
       };
       auto issue_back = [&](int t) -> bool {  // GEMM3, GEMM4, GEMM5 of tile t
-        if (!mbar_wait(p_full, t & 1, a.err)) return false;
-        const int s = t % NAT, r = L::KMAJ ? t % TR : 0;
+        if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, a.err)) return false;
+        const int s = t % NAT, r = L::KMAJ ? t % TR : 0, pb = t % PB;
+        const uint32_t t_p = tmem + L::T_P + pb * L::PCOLS;  // P^T (A operand in TMEM)
+        const uint32_t t_ds = tmem + L::T_DS + pb * BM;       // dS'^T (fp32)
         if constexpr (L::KMAJ) {
           if (!mbar_wait(&tr_full[r], (t / TR) & 1, a.err)) return false;
         }
         tc_fence_after();
+        uint64_t bdo0, bq0;
+        if constexpr (L::KMAJ) {  // transposed tiles [D rows][BM], K-major
+          bdo0 = adv(dDOT0, r * L::Q_BYTES);
+          bq0 = adv(dQT0, r * L::Q_BYTES);
+        } else {  // natural tiles [BM rows][D] read MN-major
+          bdo0 = adv(mDO0, s * L::Q_BYTES);
+          bq0 = adv(mQ0, s * L::Q_BYTES);
+        }
 #pragma unroll
         for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
-          const int kb = ks * 32;
+          const uint32_t kb = ks * 32;
           const uint32_t pa = (kb / 128) * BN * 128 + (kb % 128);
+          const uint32_t ba = L::KMAJ ? (kb / 128) * D * 128 + (kb % 128) : ks * L::KSTEP * 128;
           const uint32_t acc = (t > 0 || ks > 0) ? 1u : 0u;
-          uint64_t bdo, bq;
-          if constexpr (L::KMAJ) {  // transposed tiles [D rows][BM], K-major
-            const uint32_t ta = (kb / 128) * D * 128 + (kb % 128);
-            bdo = sw128_desc(smem_u32(smem + L::OFF_DOT + r * L::Q_BYTES) + ta, 16, 1024);
-            bq = sw128_desc(smem_u32(smem + L::OFF_QT + r * L::Q_BYTES) + ta, 16, 1024);
-          } else {  // natural tiles [BM rows][D] read MN-major
-            const uint32_t ra = ks * L::KSTEP * 128;
-            bdo = sw128_desc(smem_u32(smem + L::OFF_DO + s * L::Q_BYTES) + ra, BM * 128, 1024);
-            bq = sw128_desc(smem_u32(smem + L::OFF_Q + s * L::Q_BYTES) + ra, BM * 128, 1024);
+          // 8 TMEM columns hold one K step (8 tf32, or 16 bf16 packed in pairs)
+          mma_ts<BF16>(tmem + L::T_DV, t_p + ks * 8, adv(bdo0, ba), id_acc, acc);
+          if constexpr (L::KMAJ) {
+            mma_ts<BF16>(tmem + L::T_DK, t_ds + ks * 8, adv(bq0, ba), id_acc, acc);
+          } else {
+            mma_ss<BF16>(tmem + L::T_DK, adv(dS, pa), adv(bq0, ba), id_acc, acc);
           }
-          mma_ss<BF16>(tmem + L::T_DV, sw128_desc(sP + pa, 16, 1024), bdo, id_acc, acc);
-          mma_ss<BF16>(tmem + L::T_DK, sw128_desc(sdS + pa, 16, 1024), bq, id_acc, acc);
         }
         if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
           if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T, both K-major over keys
-            const int kb = ks * 32;
+            const uint32_t kb = ks * 32;
             const uint32_t ka = (kb / 128) * D * 128 + (kb % 128);
-            const uint32_t na = (kb / 128) * BM * 128 + (kb % 128);
-            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sKT + ka, 16, 1024),
-                         sw128_desc(sdSN + na, 16, 1024), id_dq, ks > 0);
+            const uint32_t na = pb * L::P_BYTES + (kb / 128) * BM * 128 + (kb % 128);
+            mma_ss<BF16>(tmem + L::T_DQ, adv(dKT, ka), adv(dSN, na), id_dq, ks > 0);
           } else if constexpr (L::DQT) {
             const uint32_t ra = ks * L::KSTEP * 128;
-            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sK + ra, BN * 128, 1024),
-                         sw128_desc(sdS + ra, BN * 128, 1024), id_dq, ks > 0);
+            mma_ss<BF16>(tmem + L::T_DQ, adv(mK, ra), adv(mS, ra), id_dq, ks > 0);
           } else {
             const uint32_t ra = ks * L::KSTEP * 128;
-            mma_ss<BF16>(tmem + L::T_DQ, sw128_desc(sdS + ra, BN * 128, 1024),
-                         sw128_desc(sK + ra, BN * 128, 1024), id_dq, ks > 0);
+            mma_ss<BF16>(tmem + L::T_DQ, adv(mS, ra), adv(mK, ra), id_dq, ks > 0);
           }
         }
         mma_commit(mma5_done);
+        mma_commit(&mma5_par[pb]);
         if constexpr (L::KMAJ) {
           mma_commit(&tr_empty[r]);
         } else {
@@ -461,13 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kj = w.k0 + (j >= 0 ? j : 0);
     const bool key_ok = j >= 0 && kj < a.Sk;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint8_t* sP = smem + L::OFF_P;
     uint8_t* sdS = smem + L::OFF_DS;
     uint8_t* sdSN = smem + L::OFF_DSN;
     const int cbeg = half * L::COLS;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int b = t % NSB, rs = t % RST;
+      const int b = t % NSB, rs = t % RST, pb = t % PB;
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
@@ -484,6 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* mrow = a.has_mask ? a.mask + w.b * a.msb + h * a.msh + (long long)kj * a.msk
                                      : nullptr;
       const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
+      const uint32_t t_p = tmem + lane_base + L::T_P + pb * L::PCOLS;
+      const uint32_t t_ds = tmem + lane_base + L::T_DS + pb * BM;
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + L::COLS; c0 += 16) {
         uint32_t rs16[16], rd16[16];
@@ -495,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&s_free[b]);
         }
         float pm[16], ds[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
         if (j >= 0) {
           if (plain) {
 #pragma unroll
@@ -505,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                const float p = ex2_approx(fmaf(__uint_as_float(rs16[c + u]), a.scale_log2e, -lv[u]));
+                const float p =
+                    ex2_approx(fmaf(__uint_as_float(rs16[c + u]), a.scale_log2e, -lv[u]));
                 pm[c + u] = p;
                 ds[c + u] = (p * a.scale) * (__uint_as_float(rd16[c + u]) - dv[u]);
               }
@@ -545,53 +597,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // the previous tile's GEMM3-5 must be done with the shared P / dS' tiles
-        if (c0 == cbeg && t > 0 && !warp_wait(mma5_done, (t - 1) & 1, a.err)) {
+        // GEMM3-5 of tile t - PB must be done with this tile's P / dS' buffers
+        if (c0 == cbeg && t >= PB &&
+            !warp_wait(&mma5_par[pb], ((t / PB) - 1) & 1, a.err)) {
           ok = false;
           break;
         }
-        if (j < 0) continue;  // lane holds no key row (M = 64 layout)
-        // 16 columns of row j into the swizzled P^T / dS'^T tiles [BN rows][BM]
-        const int blk = c0 / W;
-        const int pos = (c0 % W) * E;
+        tc_fence_after();
+        // P^T (and, for fp32, dS'^T) into tensor memory: the A operands of
+        // GEMM3 / GEMM4.  Whole warps: tcgen05.st is warp-collective.
         if constexpr (BF16) {
+          uint32_t pk[8];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
-            st_shared_v4(smem_u32(sP + off), pack_bf16(pm[h2 * 8 + 0], pm[h2 * 8 + 1]),
-                         pack_bf16(pm[h2 * 8 + 2], pm[h2 * 8 + 3]),
-                         pack_bf16(pm[h2 * 8 + 4], pm[h2 * 8 + 5]),
-                         pack_bf16(pm[h2 * 8 + 6], pm[h2 * 8 + 7]));
-            st_shared_v4(smem_u32(sdS + off), pack_bf16(ds[h2 * 8 + 0], ds[h2 * 8 + 1]),
-                         pack_bf16(ds[h2 * 8 + 2], ds[h2 * 8 + 3]),
-                         pack_bf16(ds[h2 * 8 + 4], ds[h2 * 8 + 5]),
-                         pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
-          }
+          for (int c = 0; c < 8; ++c) pk[c] = pack_bf16(pm[2 * c], pm[2 * c + 1]);
+          tmem_st8(t_p + c0 / 2, pk);
         } else {
-          uint32_t dsr[16];
+          uint32_t pr[16], dr[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dsr[c] = to_tf32(ds[c]);
-#pragma unroll
-          for (int h4 = 0; h4 < 4; ++h4) {
-            const uint32_t off = sw_off(blk, BN, j, pos + h4 * 16);
-            st_shared_v4(smem_u32(sP + off), to_tf32(pm[h4 * 4 + 0]), to_tf32(pm[h4 * 4 + 1]),
-                         to_tf32(pm[h4 * 4 + 2]), to_tf32(pm[h4 * 4 + 3]));
-            st_shared_v4(smem_u32(sdS + off), dsr[h4 * 4 + 0], dsr[h4 * 4 + 1], dsr[h4 * 4 + 2],
-                         dsr[h4 * 4 + 3]);
+          for (int c = 0; c < 16; ++c) {
+            pr[c] = to_tf32(pm[c]);
+            dr[c] = to_tf32(ds[c]);
           }
-          if constexpr (L::KMAJ) {
-            // dS' also as [BM rows (queries)][BN keys] for GEMM5's K-major operand
+          tmem_st16(t_p + c0, pr);
+          tmem_st16(t_ds + c0, dr);
+          if (j >= 0) {
+            // dS' as [BM rows (queries)][BN keys] for GEMM5's K-major operand
+            uint8_t* dsn = sdSN + pb * L::P_BYTES;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const uint32_t off = sw_off(j / W, BM, c0 + c, (j % W) * 4);
-              st_shared_b32(smem_u32(sdSN + off), dsr[c]);
+              st_shared_b32(smem_u32(dsn + off), dr[c]);
+            }
+          }
+        }
+        if constexpr (BF16) {
+          if (j >= 0) {
+            // dS'^T [BN rows][BM]: GEMM4's A and GEMM5's operand
+            const int blk = c0 / W;
+            const int pos = (c0 % W) * E;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
+              st_shared_v4(smem_u32(sdS + off), pack_bf16(ds[h2 * 8 + 0], ds[h2 * 8 + 1]),
+                           pack_bf16(ds[h2 * 8 + 2], ds[h2 * 8 + 3]),
+                           pack_bf16(ds[h2 * 8 + 4], ds[h2 * 8 + 5]),
+                           pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
             }
           }
         }
       }
       if (!ok) break;
+      tmem_st_wait();
       fence_proxy_async_smem();
-      mbar_arrive(p_full);
+      tc_fence_before();
+      mbar_arrive(&p_full[t & 1]);
     }
     // --------------------------------------------------------- dK / dV epilogue
     bool have = ok && T > 0;
@@ -642,14 +701,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ warps
+    // Per tile: read the GEMM5 accumulator out of TMEM, release it, and add
+    // it into the fp32 dQ accumulator in global memory.  The transposed
+    // accumulator (dQ^T: lanes = head dim, columns = queries) is staged through
+    // shared memory as [query][d] so the adds go out as 16-byte vector
+    // atomics along each dQ row.
     const int quad = warp & 3;
+    const int tid = threadIdx.x - 384;  // 0..127
     const int r = acc_row<L::M5>(quad * 32 + lane);  // accumulator row, or -1
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* stg = reinterpret_cast<float*>(smem + L::OFF_STG);
+    const long long rstride = a.layout == 0 ? D : (long long)a.H * D;
     for (int t = 0; t < T; ++t) {
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-      if (!warp_wait(mma5_done, t & 1, a.err)) break;
+      // every dQ thread is also done reading the staging tile of tile t-1
+      if (!dq_group_all(mbar_wait(mma5_done, t & 1, a.err))) break;
       tc_fence_after();
       float v[L::N5];
 #pragma unroll
@@ -662,22 +730,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(dq_free);
+      const int nq = min(BM, a.Sq - q0);
+      float* gbase = a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
       if constexpr (L::DQT) {
-        // dQ^T: row r = d, columns = queries of the tile
-        if (r >= 0 && r < D) {
-          float* base = a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D) + r;
-          const long long rstride = a.layout == 0 ? D : (long long)a.H * D;
-          const int nq = min(BM, a.Sq - q0);
+        constexpr int STG = L::STG_D;
+#pragma unroll 1
+        for (int d0 = 0; d0 < D; d0 += STG) {
+          if (d0 > 0) dq_group_sync();  // previous pass fully read
+          if (r >= d0 && r < d0 + STG) {
 #pragma unroll
-          for (int c = 0; c < BM; ++c)
-            if (c < nq) atomicAdd(base + c * rstride, v[c]);
+            for (int c = 0; c < BM; ++c) stg[c * STG + (r - d0)] = v[c];
+          }
+          dq_group_sync();
+          constexpr int N4 = BM * STG / 4;
+#pragma unroll
+          for (int idx = tid; idx < N4; idx += kDqThreads) {
+            const int row = idx / (STG / 4), c4 = idx % (STG / 4);
+            if (row < nq) {
+              const float4 val = *reinterpret_cast<const float4*>(stg + row * STG + 4 * c4);
+              atomicAdd(reinterpret_cast<float4*>(gbase + row * rstride + d0 + 4 * c4), val);
+            }
+          }
         }
       } else {
-        // dQ: row r = query of the tile, columns = d
-        const int q = q0 + r;
-        if (r >= 0 && q < a.Sq) {
-          float4* dst =
-              reinterpret_cast<float4*>(a.dq_acc + row_offset(a.layout, w.b, h, q, a.H, a.Sq, D));
+        // dQ: row r = query of the tile, columns = d (already contiguous)
+        if (r >= 0 && r < nq) {
+          float4* dst = reinterpret_cast<float4*>(gbase + r * rstride);
 #pragma unroll
           for (int c = 0; c < D / 4; ++c)
             atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));

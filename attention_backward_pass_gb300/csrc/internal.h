@@ -72,8 +72,9 @@ __host__ __device__ __forceinline__ void query_range(int Sq, int causal, long lo
 
 unsigned int* device_error_word();
 
-attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, const void* A,
-                                const void* B, float* C, float* dump, cudaStream_t stream);
+attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, int a_tmem,
+                                const void* A, const void* B, float* C, float* dump,
+                                cudaStream_t stream);
 
 // Delta / LSE2 rows and zeroing of the dQ accumulator.
 cudaError_t launch_prep(const attn_bwd_params& p, const void* O, const void* dO, const float* LSE,

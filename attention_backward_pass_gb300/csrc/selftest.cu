@@ -24,7 +24,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int blk, int rows, int row, int
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, int a_mn, int b_mn,
+__global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, int a_mn, int b_mn, int a_tmem,
                                                            const void* __restrict__ A,
                                                            const void* __restrict__ B,
                                                            float* __restrict__ C,
@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
   }
   uint32_t ncols = 32;
   while ((int)ncols < N) ncols <<= 1;
+  if (a_tmem) ncols = 512;  // A at column 256
   if (warp == 0) {
     tmem_alloc(&tmem_base, ncols);
     tmem_relinquish();
@@ -75,13 +76,43 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  if (a_tmem) {
+    // A [M][K] into TMEM: row m in the lane that holds accumulator row m,
+    // K along 32-bit columns (two bf16 per column)
+    const int lane128 = warp * 32 + (tid & 31);
+    int row = -1;
+    if (M == 128) row = lane128;
+    else if ((lane128 & 31) < 16) row = (lane128 >> 5) * 16 + (lane128 & 15);
+    const int kcols = BF16 ? K / 2 : K;
+    for (int c0 = 0; c0 < kcols; c0 += 16) {
+      uint32_t r[16];
+      for (int c = 0; c < 16; ++c) {
+        uint32_t v = 0;
+        if (row >= 0 && row < M) {
+          if constexpr (BF16) {
+            const uint16_t lo = *reinterpret_cast<const uint16_t*>(&gA[row * K + 2 * (c0 + c)]);
+            const uint16_t hi = *reinterpret_cast<const uint16_t*>(&gA[row * K + 2 * (c0 + c) + 1]);
+            v = (uint32_t)lo | ((uint32_t)hi << 16);
+          } else {
+            v = __float_as_uint(*reinterpret_cast<const float*>(&gA[row * K + c0 + c]));
+          }
+        }
+        r[c] = v;
+      }
+      tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + 256 + c0, r);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 
   if (warp == 1 && elect_one_sync()) {
     const uint32_t idesc = make_idesc(BF16, M, N, a_mn != 0, b_mn != 0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
     constexpr int KSTEP = 32 / E;  // elements of K per instruction (32 bytes)
     for (int ks = 0; ks < K / KSTEP; ++ks) {
-      uint64_t ad, bd;
+      uint64_t ad = 0, bd;
       if (a_mn) {
         ad = sw128_desc(a0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u);
       } else {
@@ -94,7 +125,12 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
         const int kb = ks * 32;
         bd = sw128_desc(b0 + (kb / 128) * N * 128 + (kb % 128), 16u, 1024u);
       }
-      mma_ss<BF16>(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      if (a_tmem) {
+        // KSTEP elements of K = 8 columns (fp32) or 8 columns of bf16 pairs
+        mma_ts<BF16>(tmem, tmem + 256 + ks * 8, bd, idesc, ks > 0 ? 1u : 0u);
+      } else {
+        mma_ss<BF16>(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      }
     }
     mma_commit(&bar);
   }
@@ -129,14 +165,16 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
 
 }  // namespace
 
-attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, const void* A,
-                                const void* B, float* C, float* dump, cudaStream_t stream) {
+attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, int a_tmem,
+                                const void* A, const void* B, float* C, float* dump,
+                                cudaStream_t stream) {
   const int W = dtype == ATTN_BF16 ? 64 : 32;
   if (!(M == 64 || M == 128)) return ATTN_ERR_INVALID;
   if (N < 16 || N > kMaxDim || N % 16 != 0) return ATTN_ERR_INVALID;
   if (K < W || K > 128 || K % W != 0) return ATTN_ERR_INVALID;
   if ((a_mn && M % W) || (b_mn && N % W)) return ATTN_ERR_INVALID;
   if (!A || !B || !C) return ATTN_ERR_INVALID;
+  if (a_tmem && (a_mn || N > 256)) return ATTN_ERR_INVALID;
   unsigned int* err = device_error_word();
   if (!err) return ATTN_ERR_CUDA;
   const size_t smem = 1024 + 65536 + 131072;
@@ -145,14 +183,16 @@ attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_
     e = cudaFuncSetAttribute(selftest_mma_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) {
-      selftest_mma_kernel<true><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, A, B, C, dump, err);
+      selftest_mma_kernel<true><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, a_tmem, A, B, C,
+                                                          dump, err);
       e = cudaGetLastError();
     }
   } else {
     e = cudaFuncSetAttribute(selftest_mma_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) {
-      selftest_mma_kernel<false><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, A, B, C, dump, err);
+      selftest_mma_kernel<false><<<1, 128, smem, stream>>>(M, N, K, a_mn, b_mn, a_tmem, A, B, C,
+                                                           dump, err);
       e = cudaGetLastError();
     }
   }

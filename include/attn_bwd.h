@@ -241,13 +241,15 @@ attn_status attn_bwd_check_device_error(int32_t clear_it);
  *   dtype: ATTN_F32 (TF32) or ATTN_BF16; A and B are fp32 or bf16 row-major
  *   host layouts [M][K] / [N][K]; a_mn / b_mn = 1 stage the operand in
  *   MN-major form (transposed tile) instead of K-major.
+ *   a_tmem = 1 takes A from tensor memory instead (row m in the lane of
+ *   accumulator row m, K along 32-bit columns, two bf16 per column).
  *   M in {64, 128}, N in {32, 64, 128, 256} (N <= 256), K a multiple of the
  *   tile width (32 fp32 / 64 bf16) and <= 128.
  *   tmem_dump (optional, fp32 [128][N]): raw accumulator contents, lane-major.
  */
 attn_status attn_selftest_mma(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t a_mn,
-                              int32_t b_mn, const void* A, const void* B, float* C,
-                              float* tmem_dump, void* stream);
+                              int32_t b_mn, int32_t a_tmem, const void* A, const void* B,
+                              float* C, float* tmem_dump, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status s);
