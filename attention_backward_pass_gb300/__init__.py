@@ -185,9 +185,9 @@ def attn_bwd_finish(p, dQ, workspace, stream=None):
 
 
 def kernels_per_call(p) -> int:
-    """Kernels one attn_bwd call launches (prep, 3 transposes for fp32, tile
-    kernel, bf16 dQ conversion)."""
-    return 1 + (3 if p.dtype == ATTN_F32 else 0) + 1 + (1 if p.dtype == ATTN_BF16 else 0)
+    """Kernels one attn_bwd call launches (prepare, tile kernel, and for bf16
+    the dQ conversion)."""
+    return 1 + 1 + (1 if p.dtype == ATTN_BF16 else 0)
 
 
 def make_decode_params(p) -> AttnBwdDecodeParams:

@@ -222,18 +222,16 @@ attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void
   if (st != ATTN_OK) return st;
   if (!all_aligned({Q, K, O, dO, LSE})) return ATTN_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
-  if (launch_prep(*p, O, dO, LSE, pl.delta, pl.lse2, pl.wl.sq_pad, pl.dq_acc, stream) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (p->dtype != ATTN_BF16 &&
-      (launch_transpose(static_cast<const float*>(Q), pl.qt, p->batch, p->num_heads, p->seq_q,
-                        p->head_dim, pl.wl.sq_pad, p->layout, stream) != cudaSuccess ||
-       launch_transpose(static_cast<const float*>(dO), pl.dot, p->batch, p->num_heads, p->seq_q,
-                        p->head_dim, pl.wl.sq_pad, p->layout, stream) != cudaSuccess ||
-       launch_transpose(static_cast<const float*>(K), pl.kt, p->batch, p->num_kv_heads, p->seq_k,
-                        p->head_dim, pl.wl.sk_pad, p->layout, stream) != cudaSuccess))
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  cudaError_t e;
+  if (p->dtype == ATTN_BF16) {
+    e = launch_prep(*p, O, dO, LSE, pl.delta, pl.lse2, pl.wl.sq_pad, pl.dq_acc, stream);
+  } else {
+    e = launch_prep_f32(*p, static_cast<const float*>(Q), static_cast<const float*>(K),
+                        static_cast<const float*>(O), static_cast<const float*>(dO), LSE, pl.delta,
+                        pl.lse2, pl.dq_acc, pl.qt, pl.dot, pl.kt, pl.wl.sq_pad, pl.wl.sk_pad,
+                        stream);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,

@@ -165,10 +165,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+// Round to TF32 (nearest, ties away from zero in magnitude) by adding half
+// a TF32 unit to the bit pattern; the tensor cores ignore the low 13 bits.
+// Same result as cvt.rna.tf32.f32 for every finite value, on the ALU pipe.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x) + 0x1000u; }
+
+// packed fp32x2 arithmetic (sm_100+)
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
   return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -510,8 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = j >= 0 && kj < a.Sk;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint8_t* sdS = smem + L::OFF_DS;
-    uint8_t* sdSN = smem + L::OFF_DSN;
     const int cbeg = half * L::COLS;
+    // fp32: this lane's column j of the swizzled dS' tile [BM rows][BN keys]:
+    // row r lives at base + r * 128 + xo[r & 7]
+    const int jj = j >= 0 ? j : 0;
+    const uint32_t dsn_lane = smem_u32(smem + L::OFF_DSN) + (jj / W) * BM * 128 + ((jj % W) * 4 & 15);
+    uint32_t xo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xo[k] = (uint32_t)(((((jj % W) * 4) >> 4) ^ k) << 4);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int b = t % NSB, rs = t % RST, pb = t % PB;
@@ -548,19 +578,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
         if (j >= 0) {
           if (plain) {
+            // two queries at a time with packed fp32x2 arithmetic
+            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c0);
+            const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
+            const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
+            const uint64_t sc2 = pk2(a.scale, a.scale);
 #pragma unroll
-            for (int c = 0; c < 16; c += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(sLSE + c0 + c);
-              const float4 d4 = *reinterpret_cast<const float4*>(sDelta + c0 + c);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float p =
-                    ex2_approx(fmaf(__uint_as_float(rs16[c + u]), a.scale_log2e, -lv[u]));
-                pm[c + u] = p;
-                ds[c + u] = (p * a.scale) * (__uint_as_float(rd16[c + u]) - dv[u]);
-              }
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
+                                           __uint_as_float(rs16[2 * i + 1])),
+                                       c2, nl2[i]);
+              float x0, x1;
+              up2(x, x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const uint64_t d = f2mul(f2mul(pk2(p0, p1), sc2),
+                                       f2sub(pk2(__uint_as_float(rd16[2 * i]),
+                                                 __uint_as_float(rd16[2 * i + 1])),
+                                             dl2[i]));
+              pm[2 * i] = p0;
+              pm[2 * i + 1] = p1;
+              up2(d, ds[2 * i], ds[2 * i + 1]);
             }
           } else {
             uint32_t words[4] = {0u, 0u, 0u, 0u};
@@ -577,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vis = m > -1.0e30f;
                 bias = m * kLog2e;
               }
-              const float x = fmaf(__uint_as_float(rs16[c]), a.scale_log2e, bias - sLSE[c0 + c]);
+              const float x = fmaf(__uint_as_float(rs16[c]), a.scale_log2e, bias + sLSE[c0 + c]);
               const float p = vis ? ex2_approx(x) : 0.f;
               float mult = 1.f;
               if (a.dropout) {
@@ -622,12 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(t_ds + c0, dr);
           if (j >= 0) {
             // dS' as [BM rows (queries)][BN keys] for GEMM5's K-major operand
-            uint8_t* dsn = sdSN + pb * L::P_BYTES;
+            const uint32_t rowbase = dsn_lane + pb * L::P_BYTES + c0 * 128;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint32_t off = sw_off(j / W, BM, c0 + c, (j % W) * 4);
-              st_shared_b32(smem_u32(dsn + off), dr[c]);
-            }
+            for (int c = 0; c < 16; ++c) st_shared_b32(rowbase + c * 128 + xo[c & 7], dr[c]);
           }
         }
         if constexpr (BF16) {

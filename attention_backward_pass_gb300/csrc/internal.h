@@ -31,7 +31,7 @@ struct TileArgs {
   uint32_t drop_threshold;  // keep iff philox word >= threshold
   float drop_inv_keep;      // 1 / (1 - p)
   uint32_t seed_lo, seed_hi;
-  const float* lse2;   // [B*H][sq_pad]  LSE * log2(e), +inf in padding rows
+  const float* lse2;   // [B*H][sq_pad]  -LSE * log2(e), -inf in padding rows
   const float* delta;  // [B*H][sq_pad]  rowsum(dO * O), 0 in padding rows
   float* dq_acc;       // fp32 dQ accumulator, same layout as dQ (dQ itself for fp32)
   void* dK;
@@ -92,9 +92,11 @@ cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const Ti
 int dkdv_block_m(int dtype, int head_dim);
 int dkdv_block_n(int dtype, int head_dim);
 
-// XT[(b*Hx + h)][d][s] (row stride s_pad) = X[b, h, s, d] for fp32 X in `layout`.
-cudaError_t launch_transpose(const float* X, float* XT, int B, int Hx, int S, int D, int s_pad,
-                             int layout, cudaStream_t stream);
+// fp32 prepare in one pass: Delta, -LSE*log2(e), zeroed dQ, Q^T, dO^T, K^T.
+cudaError_t launch_prep_f32(const attn_bwd_params& p, const float* Q, const float* K,
+                            const float* O, const float* dO, const float* LSE, float* delta,
+                            float* nlse, float* dq, float* qt, float* dot, float* kt, int sq_pad,
+                            int sk_pad, cudaStream_t stream);
 
 uint32_t dropout_threshold(float prob);
 cudaError_t launch_dropout_mask(const attn_bwd_params& p, int b, int h, uint8_t* keep,
