@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
         if (j >= 0) {
-          if (plain) {
+          if (!a.has_mask && !a.dropout) {
             // two queries at a time with packed fp32x2 arithmetic
             const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c0);
             const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
@@ -598,6 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               pm[2 * i] = p0;
               pm[2 * i + 1] = p1;
               up2(d, ds[2 * i], ds[2 * i + 1]);
+            }
+            if (!plain) {
+              // tiles that straddle the causal diagonal, the window edge or the
+              // sequence ends: zero the pairs the visibility rule excludes
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int q = q0 + c0 + c;
+                const int qa = q + (int)a.causal_offset;
+                bool vis = (q < a.Sq) && key_ok;
+                if (a.causal) vis = vis && (kj <= qa);
+                if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
+                pm[c] = vis ? pm[c] : 0.f;
+                ds[c] = vis ? ds[c] : 0.f;
+              }
             }
           } else {
             uint32_t words[4] = {0u, 0u, 0u, 0u};
