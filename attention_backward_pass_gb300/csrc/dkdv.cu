@@ -614,22 +614,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
+            // additive mask and / or dropout: per-pair exponent addend
+            // (-inf for invisible or hard-masked pairs) and multiplier, then
+            // the same packed arithmetic as above
+            float add[16], mul[16];
             uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int q = q0 + c0 + c;
-              bool vis = (q < a.Sq) && key_ok;
               const int qa = q + (int)a.causal_offset;
+              bool vis = (q < a.Sq) && key_ok;
               if (a.causal) vis = vis && (kj <= qa);
               if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
-              float bias = 0.f;
+              float ad = sLSE[c0 + c];
               if (a.has_mask && vis) {
                 const float m = __ldg(mrow + (long long)q * a.msq);
                 vis = m > -1.0e30f;
-                bias = m * kLog2e;
+                ad = fmaf(m, kLog2e, ad);
               }
-              const float x = fmaf(__uint_as_float(rs16[c]), a.scale_log2e, bias + sLSE[c0 + c]);
-              const float p = vis ? ex2_approx(x) : 0.f;
+              add[c] = vis ? ad : __int_as_float(0xff800000);
               float mult = 1.f;
               if (a.dropout) {
                 // one Philox call per 4 consecutive queries of this key
@@ -643,8 +646,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
               }
-              pm[c] = p * mult;
-              ds[c] = (p * a.scale) * (__uint_as_float(rd16[c]) * mult - sDelta[c0 + c]);
+              mul[c] = mult;
+            }
+            const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
+            const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
+            const uint64_t sc2 = pk2(a.scale, a.scale);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
+                                           __uint_as_float(rs16[2 * i + 1])),
+                                       c2, pk2(add[2 * i], add[2 * i + 1]));
+              float x0, x1;
+              up2(x, x0, x1);
+              const uint64_t p2 = pk2(ex2_approx(x0), ex2_approx(x1));
+              const uint64_t m2 = pk2(mul[2 * i], mul[2 * i + 1]);
+              const uint64_t dp2 = f2mul(pk2(__uint_as_float(rd16[2 * i]),
+                                             __uint_as_float(rd16[2 * i + 1])),
+                                         m2);
+              const uint64_t d = f2mul(f2mul(p2, sc2), f2sub(dp2, dl2[i]));
+              up2(f2mul(p2, m2), pm[2 * i], pm[2 * i + 1]);
+              up2(d, ds[2 * i], ds[2 * i + 1]);
             }
           }
         }
