@@ -46,6 +46,20 @@ struct DecArgs {
   unsigned int* err;
 };
 
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Sum G per-lane values over the warp so that the lanes of head g =
 // lane >> (5 - log2 G) all end up holding head g's total: halving exchange
 // rounds (each lane keeps the half of the heads its lane bit selects) followed
@@ -84,8 +98,9 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
   constexpr int STAGE_BYTES = 2 * kDecChunk * ROW_BYTES;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   float* stage_base = reinterpret_cast<float*>(smem_raw);  // [stages][K|V][CH][D]
-  __shared__ float w1_s[G][kDecChunk];                   // probs * dp
-  __shared__ float pr_s[G][kDecChunk];                   // probs
+  // key-major so that one vector load returns consecutive heads of a key
+  __shared__ __align__(16) float w1_s[kDecChunk][G];     // probs * dp
+  __shared__ __align__(16) float pr_s[2][kDecChunk][G];  // probs (chunk parity)
   __shared__ float red_s[NKG > 1 ? NKG : 1][2 * G][NKG > 1 ? D : 1];  // only used if NKG > 1
   __shared__ float sumpd_s[kDecThreads / 32][G];
   __shared__ __align__(8) uint64_t full[kDecStages];
@@ -114,7 +129,14 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
     float* vs = ks + kDecChunk * D;
     if (lane == 0) mbar_expect_tx(&full[s], 2u * rows * ROW_BYTES);
     __syncwarp();
-    if (lane < rows) {
+    if (a.n_kv == 1) {
+      // the chunk's rows are contiguous: one copy per tensor
+      if (lane == 0) {
+        const size_t row = (size_t)seq * a.hist + j0;
+        bulk_load(ks, a.k + row * D, rows * ROW_BYTES, &full[s]);
+        bulk_load(vs, a.v + row * D, rows * ROW_BYTES, &full[s]);
+      }
+    } else if (lane < rows) {
       const size_t row = ((size_t)seq * a.hist + j0 + lane) * a.n_kv + kv;
       bulk_load(ks + lane * D, a.k + row * D, ROW_BYTES, &full[s]);
       bulk_load(vs + lane * D, a.v + row * D, ROW_BYTES, &full[s]);
@@ -136,8 +158,23 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
   float accA[G], accB[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) accA[g] = accB[g] = 0.f;
+  uint64_t accA2[G / 2 > 0 ? G / 2 : 1], accB2[G / 2 > 0 ? G / 2 : 1];
+#pragma unroll
+  for (int i = 0; i < (G / 2 > 0 ? G / 2 : 1); ++i) accA2[i] = accB2[i] = 0;
   const int d2 = threadIdx.x % D, kg = threadIdx.x / D;
   bool ok = true;
+  // probabilities of a chunk, G x kDecChunk values, staged one chunk ahead so
+  // phase 1 never waits on a global load
+  auto load_probs = [&](int c) {
+    if (threadIdx.x < G * kDecChunk && c < nchunks) {
+      const int g = threadIdx.x / kDecChunk, jj = threadIdx.x % kDecChunk;
+      const int j = j_begin + c * kDecChunk + jj;
+      pr_s[c & 1][jj][g] =
+          j < j_end ? a.probs[((size_t)seq * a.n_heads + kv * G + g) * a.hist + j] : 0.f;
+    }
+  };
+  load_probs(0);
+  __syncthreads();
 
   for (int c = 0; c < nchunks; ++c) {
     const int s = c % kDecStages;
@@ -146,10 +183,13 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
     // keep kDecStages - 1 chunks in flight: the stage refilled here was
     // released by the __syncthreads that ended chunk c - 1
     if (warp == 0 && c + kDecStages - 1 < nchunks) issue(c + kDecStages - 1);
+    load_probs(c + 1);  // visible after this chunk's closing __syncthreads
     ok = mbar_wait(&full[s], (c / kDecStages) & 1, a.err);
     const float* ks = stage_base + (size_t)s * (STAGE_BYTES / 4);
     const float* vs = ks + kDecChunk * D;
-    // phase 1: dp for the G heads, one key per warp at a time
+    // phase 1: dp for the G heads, one key per warp at a time (unrolled so the
+    // shuffle chains of a warp's keys interleave)
+#pragma unroll
     for (int jj = warp; jj < kDecChunk; jj += kDecThreads / 32) {
       float part[G];
       if (jj < rows) {
@@ -162,12 +202,24 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
           if (k + 2 < DPL) vv[k + 2] = t.z;
           if (k + 3 < DPL) vv[k + 3] = t.w;
         }
+        if constexpr (G % 2 == 0) {
+          // two heads per packed fma
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float acc = 0.f;
+          for (int g = 0; g < G; g += 2) {
+            uint64_t acc = 0;
 #pragma unroll
-          for (int k = 0; k < DPL; ++k) acc = fmaf(dout[g][k], vv[k], acc);
-          part[g] = acc;
+            for (int k = 0; k < DPL; ++k)
+              acc = f2fma(pk2(dout[g][k], dout[g + 1][k]), pk2(vv[k], vv[k]), acc);
+            up2(acc, part[g], part[g + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) acc = fmaf(dout[g][k], vv[k], acc);
+            part[g] = acc;
+          }
         }
       } else {
 #pragma unroll
@@ -176,16 +228,14 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
       const float dp = warp_reduce_scatter<G>(part, lane);
       const int g = lane >> (5 - LOG_G);
       if ((lane & ((32 >> LOG_G) - 1)) == 0) {
-        float pr = 0.f, w1 = 0.f;
+        float w1 = 0.f;
         if (jj < rows) {
           const size_t idx = ((size_t)seq * a.n_heads + kv * G + g) * a.hist + j0 + jj;
-          pr = a.probs[idx];
-          w1 = pr * dp;
+          w1 = pr_s[c & 1][jj][g] * dp;
           a.d_scores[idx] = dp;  // parked; finalize turns it into d_scores
           sumpd_part += w1;
         }
-        w1_s[g][jj] = w1;
-        pr_s[g][jj] = pr;
+        w1_s[jj][g] = w1;
       }
     }
     // block-uniform exit if any thread's wait gave up (error path only)
@@ -193,18 +243,38 @@ __global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerS
       ok = false;
       break;
     }
-    // phase 2: A += (probs dp) k, B += probs k, thread per d
+    // phase 2: A += (probs dp) k, B += probs k, thread per d; heads in pairs
+    // with packed fma, weights of a key read as vectors (keys past `rows`
+    // carry zero weights)
     for (int jj = kg; jj < rows; jj += NKG) {
       const float kval = ks[jj * D + d2];
+      if constexpr (G % 2 == 0) {
+        const uint64_t k2 = pk2(kval, kval);
+        const uint64_t* w2 = reinterpret_cast<const uint64_t*>(&w1_s[jj][0]);
+        const uint64_t* p2 = reinterpret_cast<const uint64_t*>(&pr_s[c & 1][jj][0]);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        accA[g] = fmaf(w1_s[g][jj], kval, accA[g]);
-        accB[g] = fmaf(pr_s[g][jj], kval, accB[g]);
+        for (int i = 0; i < G / 2; ++i) {
+          accA2[i] = f2fma(w2[i], k2, accA2[i]);
+          accB2[i] = f2fma(p2[i], k2, accB2[i]);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          accA[g] = fmaf(w1_s[jj][g], kval, accA[g]);
+          accB[g] = fmaf(pr_s[c & 1][jj][g], kval, accB[g]);
+        }
       }
     }
     __syncthreads();  // stage s and w1_s / pr_s are free again
   }
 
+  if constexpr (G % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) {
+      up2(accA2[i], accA[2 * i], accA[2 * i + 1]);
+      up2(accB2[i], accB[2 * i], accB[2 * i + 1]);
+    }
+  }
   // per-warp sum_pd partials -> smem
   {
     const int g = lane >> (5 - LOG_G);
