@@ -425,10 +425,11 @@ def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
-def read_traffic(workload):
-    """DRAM bytes per launch of the tile kernel from the committed ncu summary
-    (profiles/dkdv_<workload>.md, line 'traffic_bytes_per_launch: N'), or None."""
-    path = os.path.join(ROOT, "profiles", f"dkdv_{workload}.md")
+def read_traffic(workload, prefix="dkdv_"):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/<prefix><workload>.md, line 'traffic_bytes_per_launch: N'),
+    or None when there is no summary for this workload."""
+    path = os.path.join(ROOT, "profiles", f"{prefix}{workload}.md")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -518,7 +519,8 @@ def run_decode(args):
                        "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": nbytes / (mean_ms * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s",
-                         "frac": nbytes / (mean_ms * 1e-3) / 1e9 / peak, "traffic": None,
+                         "frac": nbytes / (mean_ms * 1e-3) / 1e9 / peak,
+                         "traffic": read_traffic("main", prefix="decode_"),
                          "kernel": "decode_main_kernel + decode_finalize_kernel",
                          "peak_source": f"{src} hbm_gbs"},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clocks,
