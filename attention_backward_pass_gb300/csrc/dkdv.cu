@@ -26,16 +26,18 @@
 //    (GEMM3/4) travel in separate rings, so a natural stage is released as
 //    soon as GEMM1/2 are done with it.
 //
-// Pipeline.  GEMM1/2 of tile t are issued as soon as the softmax warps have
-// read tile t-NSB's scores out of tensor memory (NSB = 1 or 2 score
-// buffers), GEMM3-5 of tile t-1 right after; the softmax warps compute tile t
-// while the tensor cores finish tile t-1 and start tile t+1, and only wait
-// for GEMM3-5 of t-1 before overwriting the shared P / dS' tiles.
+// Pipeline.  GEMM1/2 of tile t + NSB are issued as soon as the softmax warps
+// have read tile t's scores out of tensor memory (NSB = 1 or 2 score
+// buffers), then GEMM3-5 of tile t once its P / dS' are written; the softmax
+// warps compute tile t while the tensor cores finish earlier tiles and start
+// later ones, and only wait for GEMM3-5 of tile t - PB (PB = 1 or 2 P / dS'
+// buffers) before overwriting P / dS'.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer
+//   warp 0       TMA producer: resident key tiles, natural Q / dO ring
 //   warp 1       MMA issuer (one elected lane)
 //   warp 2       TMEM allocator
+//   warp 3       TMA producer of the transposed ring (fp32)
 //   warps 4-11   softmax: warp w serves TMEM sub-partition w % 4 (its key
 //                rows) and half (w - 4) / 4 of the query columns; turns S^T
 //                and dP^T into P o M and dS', stores them as MMA operands, and
@@ -102,19 +104,20 @@ struct Layout {
   // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
   static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
   static constexpr int OFF_DSN = OFF_DS + (KMAJ ? 0 : P_BYTES);
-  static constexpr int ROW_ST = KMAJ ? TR : NAT;  // ring that carries LSE2 / Delta
+  static constexpr int ROW_ST = 4;  // stages of the LSE2 / Delta ring
   static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? PB * P_BYTES : 0);
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
   static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
   static constexpr int OFF_BAR = OFF_STG + BM * STG_D * 4;
-  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * NSB + 2 + PB + 6;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 2 * NSB + 2 + PB + 6;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
-  static constexpr int NAT_TX = 2 * Q_BYTES + (KMAJ ? 0 : 2 * BM * 4);
-  static constexpr int TR_TX = 2 * Q_BYTES + 2 * BM * 4;
+  static constexpr int NAT_TX = 2 * Q_BYTES;
+  static constexpr int TR_TX = 2 * Q_BYTES;
+  static constexpr int ROW_TX = 2 * BM * 4;
   static constexpr int KV_TX = (KMAJ ? 3 : 2) * K_BYTES;
   // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
   static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
@@ -298,7 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* nat_empty = nat_full + NAT;      // [NAT] natural stage free (MMA commit)
   uint64_t* tr_full = nat_empty + NAT;       // [TR] transposed tiles + LSE2/Delta landed
   uint64_t* tr_empty = tr_full + TR;         // [TR] transposed stage free (MMA commit)
-  uint64_t* s_full = tr_empty + TR;          // [NSB] GEMM1/2 done into score buffer b
+  uint64_t* row_full = tr_empty + TR;        // [ROW_ST] LSE2 / Delta of a tile landed
+  uint64_t* row_empty = row_full + L::ROW_ST;  // [ROW_ST] softmax warps done with them
+  uint64_t* s_full = row_empty + L::ROW_ST;  // [NSB] GEMM1/2 done into score buffer b
   uint64_t* s_free = s_full + NSB;           // [NSB] softmax warps have read buffer b
   uint64_t* p_full = s_free + NSB;           // [2] P / dS' of a tile written (by parity)
   uint64_t* mma5_par = p_full + 2;           // [PB] GEMM3/4/5 of a tile done (by t % PB)
@@ -308,8 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_done = kv_full + 3;          // all products done
   uint64_t* final_bar = kv_full + 4;         // unwinding: products in flight done
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
-  // the ring whose stage carries LSE2 / Delta of a tile, and its depth
-  uint64_t* row_full = L::KMAJ ? tr_full : nat_full;
   constexpr int RST = L::ROW_ST;
 
   const int warp = threadIdx.x >> 5;
@@ -325,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < TR; ++s) {
       mbar_init(&tr_full[s], 1);
       mbar_init(&tr_empty[s], 1);
+    }
+    for (int s = 0; s < L::ROW_ST; ++s) {
+      mbar_init(&row_full[s], 1);
+      mbar_init(&row_empty[s], kSoftmaxThreads);
     }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&s_full[s], 1);
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + L::OFF_KT + cb * D * 128, &tm_kt, kv_full, w.k0 + cb * W, 0, bhkv,
                       0);
       }
-      int nat_issued = 0, tr_issued = 0;
+      int nat_issued = 0, row_issued = 0;
       for (int t = 0; t < T; ++t) {
         const int g = t / w.tiles_per_head;
         const int h = w.kvh * a.group + g;
@@ -385,13 +392,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + L::OFF_DO + s * L::Q_BYTES + cb * BM * 128, &tm_do, &nat_full[s],
                       cb * W, q0, h, w.b);
         }
-        if constexpr (!L::KMAJ) {
-          bulk_load(smem + L::OFF_LSE + s * BM * 4, a.lse2 + row, BM * 4, &nat_full[s]);
-          bulk_load(smem + L::OFF_DELTA + s * BM * 4, a.delta + row, BM * 4, &nat_full[s]);
-        }
         nat_issued = t + 1;
-        if constexpr (L::KMAJ) {
-          // transposed Q^T / dO^T tiles [D rows][BM] and LSE2 / Delta
+        // LSE2 / Delta rows of the tile: a ring of their own, released by the
+        // softmax warps as soon as they finish the tile
+        const int rr = t % RST;
+        if (t >= RST && !mbar_wait(&row_empty[rr], ((t / RST) - 1) & 1, a.err)) break;
+        mbar_expect_tx(&row_full[rr], L::ROW_TX);
+        bulk_load(smem + L::OFF_LSE + rr * BM * 4, a.lse2 + row, BM * 4, &row_full[rr]);
+        bulk_load(smem + L::OFF_DELTA + rr * BM * 4, a.delta + row, BM * 4, &row_full[rr]);
+        row_issued = t + 1;
+      }
+      // let every copy still in flight land before the CTA can exit
+      drain_wait(kv_full, 0);
+      for (int t = (nat_issued > NAT ? nat_issued - NAT : 0); t < nat_issued; ++t)
+        drain_wait(&nat_full[t % NAT], (t / NAT) & 1);
+      for (int t = (row_issued > RST ? row_issued - RST : 0); t < row_issued; ++t)
+        drain_wait(&row_full[t % RST], (t / RST) & 1);
+    }
+    __syncwarp();  // reconverge before the block-wide barrier at the end
+  } else if (warp == 3) {
+    // ------------------------------------------------- transposed-tile producer
+    // (fp32) Q^T / dO^T tiles [D rows][BM] and LSE2 / Delta, in a ring of its
+    // own so it never holds up the natural tiles that GEMM1/2 wait for
+    if constexpr (L::KMAJ) {
+      if (elect_one_sync() && T > 0) {
+        tma_prefetch_desc(&tm_qt);
+        tma_prefetch_desc(&tm_dot);
+        int tr_issued = 0;
+        for (int t = 0; t < T; ++t) {
+          const int g = t / w.tiles_per_head;
+          const int h = w.kvh * a.group + g;
+          const int bh = w.b * a.H + h;
+          const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
           const int r = t % TR;
           if (t >= TR && !mbar_wait(&tr_empty[r], ((t / TR) - 1) & 1, a.err)) break;
           mbar_expect_tx(&tr_full[r], L::TR_TX);
@@ -401,21 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(smem + L::OFF_DOT + r * L::Q_BYTES + cb * D * 128, &tm_dot, &tr_full[r],
                         q0 + cb * W, 0, bh, 0);
           }
-          bulk_load(smem + L::OFF_LSE + r * BM * 4, a.lse2 + row, BM * 4, &tr_full[r]);
-          bulk_load(smem + L::OFF_DELTA + r * BM * 4, a.delta + row, BM * 4, &tr_full[r]);
           tr_issued = t + 1;
         }
-      }
-      // let every copy still in flight land before the CTA can exit
-      drain_wait(kv_full, 0);
-      for (int t = (nat_issued > NAT ? nat_issued - NAT : 0); t < nat_issued; ++t)
-        drain_wait(&nat_full[t % NAT], (t / NAT) & 1);
-      if constexpr (L::KMAJ) {
         for (int t = (tr_issued > TR ? tr_issued - TR : 0); t < tr_issued; ++t)
           drain_wait(&tr_full[t % TR], (t / TR) & 1);
       }
+      __syncwarp();
     }
-    __syncwarp();  // reconverge before the block-wide barrier at the end
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Shared-memory descriptors are built once; every product then only adds
@@ -518,11 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      // GEMM1/2 run NSB tiles ahead of GEMM3-5: front(t + NSB) only needs the
+      // softmax warps to have read tile t's scores (s_free), which happens
+      // before they finish tile t (p_full), so the tensor cores compute the
+      // next scores while the softmax warps are still busy.
+      for (int t = 0; ok && t < NSB && t < T; ++t)
+        if (!issue_front(t)) ok = false;
       for (int t = 0; ok && t < T; ++t) {
-        if (!issue_front(t)) { ok = false; break; }
-        if (t > 0 && !issue_back(t - 1)) { ok = false; break; }
+        if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
+        if (!issue_back(t)) { ok = false; break; }
       }
-      if (ok && issue_back(T - 1)) mma_commit(acc_done);
+      if (ok) mma_commit(acc_done);
       mma_commit(final_bar);
     }
     __syncwarp();  // reconverge before the block-wide barrier at the end
@@ -720,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(&row_empty[rs]);
     }
     // --------------------------------------------------------- dK / dV epilogue
     bool have = ok && T > 0;
