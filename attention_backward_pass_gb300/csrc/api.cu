@@ -116,6 +116,30 @@ CUresult make_map_t(CUtensorMap* m, const void* base, int D, int S, int s_pad, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// fp32 dQ accumulator in the problem's layout, unswizzled boxes of
+// box_d x box_rows: the TMA reduce-add target of the tile kernel.
+CUresult make_map_dq(CUtensorMap* m, void* base, int D, int S, int H, int B, int layout,
+                     int box_d, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3];
+  if (layout == ATTN_LAYOUT_BHSD) {
+    strides[0] = (cuuint64_t)D * 4;
+    strides[1] = (cuuint64_t)S * D * 4;
+    strides[2] = (cuuint64_t)H * S * D * 4;
+  } else {
+    strides[0] = (cuuint64_t)H * D * 4;
+    strides[1] = (cuuint64_t)D * 4;
+    strides[2] = (cuuint64_t)S * H * D * 4;
+  }
+  cuuint32_t box[4] = {(cuuint32_t)box_d, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int H, int B,
                   int layout, int box_rows) {
   EncodeTiledFn enc = encode_fn();
@@ -265,7 +289,9 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
       make_map(&maps.k, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
                bn) != CUDA_SUCCESS ||
       make_map(&maps.v, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
-               bn) != CUDA_SUCCESS)
+               bn) != CUDA_SUCCESS ||
+      make_map_dq(&maps.dq, pl.dq_acc, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
+                  dkdv_dq_box_d(p->dtype, p->head_dim), bm) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
 
   TileArgs a;

@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_qt,
                 const __grid_constant__ CUtensorMap tm_kt,
-                const __grid_constant__ CUtensorMap tm_dot, const TileArgs a) {
+                const __grid_constant__ CUtensorMap tm_dot,
+                const __grid_constant__ CUtensorMap tm_dq, const TileArgs a) {
   using L = Layout<BF16, D>;
   constexpr int BM = L::BM, NAT = L::NAT, TR = L::TR, NSB = L::NSB, PB = L::PB, BN = L::BN,
                 W = L::W, E = L::E;
@@ -833,25 +834,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = min(BM, a.Sq - q0);
       float* gbase = a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
       if constexpr (L::DQT) {
+        // stage [BM queries][STG d] and hand the tile to the TMA engine as one
+        // reduce-add (rows past Sq fall outside the tensor map and are skipped)
         constexpr int STG = L::STG_D;
 #pragma unroll 1
         for (int d0 = 0; d0 < D; d0 += STG) {
-          if (d0 > 0) dq_group_sync();  // previous pass fully read
+          if (tid == 0) bulk_wait_read();  // previous reduce has read the stage
+          dq_group_sync();
           if (r >= d0 && r < d0 + STG) {
 #pragma unroll
             for (int c = 0; c < BM; ++c) stg[c * STG + (r - d0)] = v[c];
           }
+          fence_proxy_async_smem();
           dq_group_sync();
-          constexpr int N4 = BM * STG / 4;
-#pragma unroll
-          for (int idx = tid; idx < N4; idx += kDqThreads) {
-            const int row = idx / (STG / 4), c4 = idx % (STG / 4);
-            if (row < nq) {
-              const float4 val = *reinterpret_cast<const float4*>(stg + row * STG + 4 * c4);
-              atomicAdd(reinterpret_cast<float4*>(gbase + row * rstride + d0 + 4 * c4), val);
-            }
+          if (tid == 0) {
+            tma_reduce_add_4d(&tm_dq, stg, d0, q0, h, w.b);
+            bulk_commit();
           }
         }
+        (void)gbase;
+        (void)nq;
       } else {
         // dQ: row r = query of the tile, columns = d (already contiguous)
         if (r >= 0 && r < nq) {
@@ -862,6 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (tid == 0) bulk_wait_all();  // reductions complete before the CTA exits
   }
 
   tc_fence_before();
@@ -882,7 +885,8 @@ cudaError_t launch_impl(const TileMaps& m, const TileArgs& a, cudaStream_t strea
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = a.n_kv_tiles * a.B * a.Hkv;
-  kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, a);
+  kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, m.dq,
+                                                  a);
   return cudaGetLastError();
 }
 
@@ -891,6 +895,15 @@ cudaError_t launch_impl(const TileMaps& m, const TileArgs& a, cudaStream_t strea
 int dkdv_block_m(int dtype, int head_dim) {
   if (dtype == ATTN_BF16) return head_dim == 64 ? Cfg<true, 64>::BM : Cfg<true, 128>::BM;
   return head_dim == 64 ? Cfg<false, 64>::BM : Cfg<false, 128>::BM;
+}
+
+int dkdv_dq_box_d(int dtype, int head_dim) {
+  int d;
+  if (dtype == ATTN_BF16)
+    d = head_dim == 64 ? Layout<true, 64>::STG_D : Layout<true, 128>::STG_D;
+  else
+    d = head_dim == 64 ? Layout<false, 64>::STG_D : Layout<false, 128>::STG_D;
+  return d > 0 ? d : 64;  // configurations without a staged dQ still get a valid map
 }
 
 int dkdv_block_n(int dtype, int head_dim) {

@@ -86,11 +86,13 @@ cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, voi
 struct TileMaps {
   CUtensorMap q, k, v, dout;  // natural [.., S, .., D] tensors
   CUtensorMap qt, kt, dot;    // transposed copies [B*H][D][S_pad] (fp32 path)
+  CUtensorMap dq;             // fp32 dQ accumulator (reduce-add target)
 };
 cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,
                         cudaStream_t stream);
 int dkdv_block_m(int dtype, int head_dim);
 int dkdv_block_n(int dtype, int head_dim);
+int dkdv_dq_box_d(int dtype, int head_dim);  // head-dim columns per dQ reduce box
 
 // fp32 prepare in one pass: Delta, -LSE*log2(e), zeroed dQ, Q^T, dO^T, K^T.
 cudaError_t launch_prep_f32(const attn_bwd_params& p, const float* Q, const float* K,
