@@ -59,25 +59,30 @@ namespace {
 
 template <bool BF16, int D>
 struct Cfg;
+// INPL: P and dS' overwrite S^T and dP^T in tensor memory (no separate P /
+// dS' columns), and the shared-memory dS' tile of query tile t is written over
+// tile t's own natural Q / dO stage (GEMM1/2 are done with it by then), which
+// is released to the producer only after GEMM5; VTM: V lives in tensor memory
+// as GEMM2's A operand, so GEMM2 reads only the dO tile from shared memory.
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
-  static constexpr int BN = 128, BM = 32, NAT = 3, TR = 2, NSB = 2, PB = 2;
-  static constexpr bool KMAJ = true, DQT = true;
+  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 1, NSB = 2, PB = 1;
+  static constexpr bool KMAJ = true, DQT = true, INPL = true, VTM = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
   static constexpr int BN = 64, BM = 32, NAT = 2, TR = 1, NSB = 2, PB = 1;
-  static constexpr bool KMAJ = true, DQT = true;
+  static constexpr bool KMAJ = true, DQT = true, INPL = false, VTM = false;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
   static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1;
-  static constexpr bool KMAJ = false, DQT = false;
+  static constexpr bool KMAJ = false, DQT = false, INPL = false, VTM = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
   static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1;
-  static constexpr bool KMAJ = false, DQT = true;
+  static constexpr bool KMAJ = false, DQT = true, INPL = false, VTM = false;
 };
 
 template <bool BF16, int D>
@@ -85,7 +90,7 @@ struct Layout {
   using C = Cfg<BF16, D>;
   static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB,
                        PB = C::PB;
-  static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT;
+  static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT, INPL = C::INPL, VTM = C::VTM;
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
   static constexpr int W = 128 / E;       // elements per 128-byte segment
   static constexpr int KSTEP = 32 / E;    // K elements per MMA instruction
@@ -96,22 +101,28 @@ struct Layout {
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + K_BYTES;  // must follow K (padded GEMM5 reads it)
-  static constexpr int OFF_KT = OFF_V + K_BYTES;
-  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);  // natural ring [NAT]
-  static constexpr int OFF_DO = OFF_Q + NAT * Q_BYTES;
-  static constexpr int OFF_QT = OFF_DO + NAT * Q_BYTES;        // transposed ring [TR]
+  static constexpr int OFF_KT = OFF_V + (VTM ? 0 : K_BYTES);
+  // natural ring [NAT]: separate Q and dO rings, or (INPL) stages of
+  // [Q tile][dO tile] that later hold the tile's dS' [BM rows][BN keys]
+  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);
+  static constexpr int NAT_STRIDE = INPL ? 2 * Q_BYTES : Q_BYTES;
+  static constexpr int OFF_DO = OFF_Q + (INPL ? Q_BYTES : NAT * Q_BYTES);
+  static constexpr int OFF_QT = OFF_Q + 2 * NAT * Q_BYTES;     // transposed ring [TR]
   static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
   // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
   static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
   static constexpr int OFF_DSN = OFF_DS + (KMAJ ? 0 : P_BYTES);
   static constexpr int ROW_ST = 4;  // stages of the LSE2 / Delta ring
-  static constexpr int OFF_LSE = OFF_DSN + (KMAJ ? PB * P_BYTES : 0);
+  static constexpr int OFF_LSE = OFF_DSN + (KMAJ && !INPL ? PB * P_BYTES : 0);
+  // VTM: V lands in the (not yet used) transposed ring and is moved into
+  // tensor memory before the first transposed tiles are fetched
+  static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
   static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
   static constexpr int OFF_BAR = OFF_STG + BM * STG_D * 4;
-  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 2 * NSB + 2 + PB + 6;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 3 * NSB + 2 + PB + 7;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
@@ -126,9 +137,11 @@ struct Layout {
   // element; bf16: two per column), fp32: PB x dS'^T, then dV, dK, dQ
   static constexpr int PCOLS = BF16 ? BM / 2 : BM;
   static constexpr int T_P = 2 * BM * NSB;
-  static constexpr int T_DS = T_P + PB * PCOLS;
-  static constexpr int T_DV = T_DS + (KMAJ ? PB * BM : 0), T_DK = T_DV + D, T_DQ = T_DK + D;
-  static constexpr int T_USED = T_DQ + N5;
+  static constexpr int T_DS = T_P + (INPL ? 0 : PB * PCOLS);
+  static constexpr int T_DV = T_DS + (KMAJ && !INPL ? PB * BM : 0), T_DK = T_DV + D,
+                       T_DQ = T_DK + D;
+  static constexpr int T_V = T_DQ + N5;
+  static constexpr int T_USED = T_V + (VTM ? D : 0);
   static constexpr int T_ALLOC = T_USED <= 256 ? 256 : 512;
   // softmax split: two warps per TMEM sub-partition, each on half the columns
   static constexpr int COLS = BM / 2;
@@ -139,6 +152,10 @@ struct Layout {
   static_assert(KMAJ || NAT >= 2, "stages are released only after GEMM3/4");
   static_assert(PB == 1 || PB == 2, "P / dS buffers");
   static_assert(BN == 64 || BN == 128, "key tile");
+  static_assert(!INPL || (KMAJ && !BF16 && NAT_STRIDE >= P_BYTES && NAT >= 3),
+                "in-place P / dS' is the fp32 layout; dS' fits a natural stage");
+  static_assert(!VTM || (INPL && BN == 128 && 2 * TR * Q_BYTES >= K_BYTES && D / W == 2),
+                "V staging through the transposed ring, one column block per softmax half");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
 
@@ -248,6 +265,7 @@ __device__ __forceinline__ void dq_group_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+
 struct TileWork {
   int b, kvh, k0, q_begin, q_end, q_first, tiles_per_head, total;
 };
@@ -313,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_free = kv_full + 2;           // dQ accumulator drained
   uint64_t* acc_done = kv_full + 3;          // all products done
   uint64_t* final_bar = kv_full + 4;         // unwinding: products in flight done
+  uint64_t* v_ready = kv_full + 5;           // (VTM) V copied into tensor memory
+  uint64_t* pfree = kv_full + 6;             // [NSB] (INPL) GEMM3/4 done with buffer b
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
   constexpr int RST = L::ROW_ST;
 
@@ -346,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_free, kDqThreads);
     mbar_init(acc_done, 1);
     mbar_init(final_bar, 1);
+    mbar_init(v_ready, kSoftmaxThreads);
+    for (int s = 0; s < NSB; ++s) mbar_init(&pfree[s], 1);
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -368,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(kv_full, L::KV_TX);
       for (int cb = 0; cb < L::NB_D; ++cb) {
         tma_load_4d(smem + L::OFF_K + cb * BN * 128, &tm_k, kv_full, cb * W, w.k0, w.kvh, w.b);
-        tma_load_4d(smem + L::OFF_V + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh, w.b);
+        tma_load_4d(smem + L::OFF_VLOAD + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh,
+                    w.b);
       }
       if constexpr (L::KMAJ) {
         // K^T [D rows][BN keys]: one box of W keys x D rows per column block
@@ -388,9 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= NAT && !mbar_wait(&nat_empty[s], ((t / NAT) - 1) & 1, a.err)) break;
         mbar_expect_tx(&nat_full[s], L::NAT_TX);
         for (int cb = 0; cb < L::NB_D; ++cb) {
-          tma_load_4d(smem + L::OFF_Q + s * L::Q_BYTES + cb * BM * 128, &tm_q, &nat_full[s],
+          tma_load_4d(smem + L::OFF_Q + s * L::NAT_STRIDE + cb * BM * 128, &tm_q, &nat_full[s],
                       cb * W, q0, h, w.b);
-          tma_load_4d(smem + L::OFF_DO + s * L::Q_BYTES + cb * BM * 128, &tm_do, &nat_full[s],
+          tma_load_4d(smem + L::OFF_DO + s * L::NAT_STRIDE + cb * BM * 128, &tm_do,
+                      &nat_full[s],
                       cb * W, q0, h, w.b);
         }
         nat_issued = t + 1;
@@ -420,7 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_qt);
         tma_prefetch_desc(&tm_dot);
         int tr_issued = 0;
-        for (int t = 0; t < T; ++t) {
+        // VTM: the first transposed tiles overwrite the staged V, so they wait
+        // until the softmax warps have moved it into tensor memory
+        const bool v_ok = !L::VTM || mbar_wait(v_ready, 0, a.err);
+        for (int t = 0; v_ok && t < T; ++t) {
           const int g = t / w.tiles_per_head;
           const int h = w.kvh * a.group + g;
           const int bh = w.b * a.H + h;
@@ -455,7 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV = sw128_desc(smem_u32(smem + L::OFF_V), 16, 1024);
       const uint64_t dS = sw128_desc(smem_u32(smem + L::OFF_DS), 16, 1024);
       const uint64_t dKT = sw128_desc(smem_u32(smem + L::OFF_KT), 16, 1024);
-      const uint64_t dSN = sw128_desc(smem_u32(smem + L::OFF_DSN), 16, 1024);
+      // fp32 dS' [BM rows][BN keys]: its own region, or (INPL) natural stage 0
+      const uint64_t dSN =
+          sw128_desc(smem_u32(smem + (L::INPL ? L::OFF_Q : L::OFF_DSN)), 16, 1024);
       const uint64_t dQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), 16, 1024);
       const uint64_t dDO0 = sw128_desc(smem_u32(smem + L::OFF_DO), 16, 1024);
       const uint64_t dQT0 = sw128_desc(smem_u32(smem + L::OFF_QT), 16, 1024);
@@ -470,9 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_front = [&](int t) -> bool {  // GEMM1, GEMM2 of tile t
         const int s = t % NAT, b = t % NSB;
         if (!mbar_wait(&nat_full[s], (t / NAT) & 1, a.err)) return false;
-        if (t >= NSB && !mbar_wait(&s_free[b], ((t / NSB) - 1) & 1, a.err)) return false;
+        // buffer b is free once the softmax warps have read its scores, or
+        // (in place) once GEMM3/4 have read the P / dS' written over them
+        if (t >= NSB &&
+            !mbar_wait(L::INPL ? &pfree[b] : &s_free[b], ((t / NSB) - 1) & 1, a.err))
+          return false;
         tc_fence_after();
-        const uint64_t dQ = adv(dQ0, s * L::Q_BYTES), dDO = adv(dDO0, s * L::Q_BYTES);
+        const uint64_t dQ = adv(dQ0, s * L::NAT_STRIDE), dDO = adv(dDO0, s * L::NAT_STRIDE);
         const uint32_t t_s = tmem + b * 2 * BM, t_dp = t_s + BM;
 #pragma unroll
         for (int ks = 0; ks < D / L::KSTEP; ++ks) {
@@ -480,17 +513,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ka = (kb / 128) * BN * 128 + (kb % 128);
           const uint32_t qa = (kb / 128) * BM * 128 + (kb % 128);
           mma_ss<BF16>(t_s, adv(dK, ka), adv(dQ, qa), id_s, ks > 0);
-          mma_ss<BF16>(t_dp, adv(dV, ka), adv(dDO, qa), id_s, ks > 0);
+          if constexpr (L::VTM) {  // V [BN lanes][D columns] in tensor memory
+            mma_ts<BF16>(t_dp, tmem + L::T_V + ks * 8, adv(dDO, qa), id_s, ks > 0);
+          } else {
+            mma_ss<BF16>(t_dp, adv(dV, ka), adv(dDO, qa), id_s, ks > 0);
+          }
         }
         mma_commit(&s_full[b]);
-        if constexpr (L::KMAJ) mma_commit(&nat_empty[s]);  // natural tiles done with
+        // natural tiles done with (INPL: the stage then holds dS' until GEMM5)
+        if constexpr (L::KMAJ && !L::INPL) mma_commit(&nat_empty[s]);
         return true;
       };
       auto issue_back = [&](int t) -> bool {  // GEMM3, GEMM4, GEMM5 of tile t
         if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, a.err)) return false;
-        const int s = t % NAT, r = L::KMAJ ? t % TR : 0, pb = t % PB;
-        const uint32_t t_p = tmem + L::T_P + pb * L::PCOLS;  // P^T (A operand in TMEM)
-        const uint32_t t_ds = tmem + L::T_DS + pb * BM;       // dS'^T (fp32)
+        const int s = t % NAT, r = L::KMAJ ? t % TR : 0, pb = t % PB, b = t % NSB;
+        // P^T and (fp32) dS'^T: A operands of GEMM3/4 in tensor memory
+        const uint32_t t_p = L::INPL ? tmem + b * 2 * BM : tmem + L::T_P + pb * L::PCOLS;
+        const uint32_t t_ds = L::INPL ? t_p + BM : tmem + L::T_DS + pb * BM;
         if constexpr (L::KMAJ) {
           if (!mbar_wait(&tr_full[r], (t / TR) & 1, a.err)) return false;
         }
@@ -500,8 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bdo0 = adv(dDOT0, r * L::Q_BYTES);
           bq0 = adv(dQT0, r * L::Q_BYTES);
         } else {  // natural tiles [BM rows][D] read MN-major
-          bdo0 = adv(mDO0, s * L::Q_BYTES);
-          bq0 = adv(mQ0, s * L::Q_BYTES);
+          bdo0 = adv(mDO0, s * L::NAT_STRIDE);
+          bq0 = adv(mQ0, s * L::NAT_STRIDE);
         }
 #pragma unroll
         for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
@@ -517,6 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss<BF16>(tmem + L::T_DK, adv(dS, pa), adv(bq0, ba), id_acc, acc);
           }
         }
+        if constexpr (L::INPL) mma_commit(&pfree[b]);  // score buffer b reusable
+        if constexpr (L::KMAJ) mma_commit(&tr_empty[r]);  // GEMM5 does not read them
         if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
         tc_fence_after();
 #pragma unroll
@@ -524,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T, both K-major over keys
             const uint32_t kb = ks * 32;
             const uint32_t ka = (kb / 128) * D * 128 + (kb % 128);
-            const uint32_t na = pb * L::P_BYTES + (kb / 128) * BM * 128 + (kb % 128);
+            const uint32_t na = (L::INPL ? s * L::NAT_STRIDE : pb * L::P_BYTES) +
+                                (kb / 128) * BM * 128 + (kb % 128);
             mma_ss<BF16>(tmem + L::T_DQ, adv(dKT, ka), adv(dSN, na), id_dq, ks > 0);
           } else if constexpr (L::DQT) {
             const uint32_t ra = ks * L::KSTEP * 128;
@@ -536,22 +578,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma5_done);
         mma_commit(&mma5_par[pb]);
-        if constexpr (L::KMAJ) {
-          mma_commit(&tr_empty[r]);
-        } else {
-          mma_commit(&nat_empty[s]);
-        }
+        if constexpr (!L::KMAJ || L::INPL) mma_commit(&nat_empty[s]);
         return true;
       };
       // GEMM1/2 run NSB tiles ahead of GEMM3-5: front(t + NSB) only needs the
       // softmax warps to have read tile t's scores (s_free), which happens
       // before they finish tile t (p_full), so the tensor cores compute the
       // next scores while the softmax warps are still busy.
+      if constexpr (L::VTM) {
+        ok = ok && mbar_wait(v_ready, 0, a.err);
+        tc_fence_after();
+      }
       for (int t = 0; ok && t < NSB && t < T; ++t)
         if (!issue_front(t)) ok = false;
       for (int t = 0; ok && t < T; ++t) {
-        if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
-        if (!issue_back(t)) { ok = false; break; }
+        if constexpr (L::INPL) {
+          // in place: buffer t % NSB is rewritten only after GEMM3/4 of tile t
+          // read it; GEMM5 of tile t keeps the tensor cores busy meanwhile
+          if (!issue_back(t)) { ok = false; break; }
+          if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
+        } else {
+          if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
+          if (!issue_back(t)) { ok = false; break; }
+        }
       }
       if (ok) mma_commit(acc_done);
       mma_commit(final_bar);
@@ -569,12 +618,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // fp32: this lane's column j of the swizzled dS' tile [BM rows][BN keys]:
     // row r lives at base + r * 128 + xo[r & 7]
     const int jj = j >= 0 ? j : 0;
-    const uint32_t dsn_lane = smem_u32(smem + L::OFF_DSN) + (jj / W) * BM * 128 + ((jj % W) * 4 & 15);
+    const uint32_t dsn_lane = (jj / W) * BM * 128 + ((jj % W) * 4 & 15);
     uint32_t xo[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) xo[k] = (uint32_t)(((((jj % W) * 4) >> 4) ^ k) << 4);
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    if constexpr (L::VTM) {
+      if (T > 0) {
+        // V into tensor memory (GEMM2's A operand): this lane's key row, this
+        // warp's column block of the swizzled tile, 32 fp32 = 32 columns
+        ok = warp_wait(kv_full, 0, a.err);
+        if (ok) {
+          const uint8_t* vrow = smem + L::OFF_VLOAD + half * BN * 128 + jj * 128;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t rv[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = h2 * 4 + c;
+              const uint4 v4 =
+                  *reinterpret_cast<const uint4*>(vrow + ((chunk ^ (jj & 7)) << 4));
+              rv[4 * c] = v4.x;
+              rv[4 * c + 1] = v4.y;
+              rv[4 * c + 2] = v4.z;
+              rv[4 * c + 3] = v4.w;
+            }
+            tmem_st16(tmem + lane_base + L::T_V + half * W + h2 * 16, rv);
+          }
+          tmem_st_wait();
+        }
+        // releases the staged V to the transposed-tile producer and tensor
+        // memory's V to the MMA issuer
+        tc_fence_before();
+        mbar_arrive(v_ready);
+      }
+    }
+    for (int t = 0; ok && t < T; ++t) {
       const int b = t % NSB, rs = t % RST, pb = t % PB;
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
@@ -592,156 +671,182 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* mrow = a.has_mask ? a.mask + w.b * a.msb + h * a.msh + (long long)kj * a.msk
                                      : nullptr;
       const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
-      const uint32_t t_p = tmem + lane_base + L::T_P + pb * L::PCOLS;
-      const uint32_t t_ds = tmem + lane_base + L::T_DS + pb * BM;
+      const uint32_t t_p = L::INPL ? t_s : tmem + lane_base + L::T_P + pb * L::PCOLS;
+      const uint32_t t_ds = L::INPL ? t_dp : tmem + lane_base + L::T_DS + pb * BM;
+      // fp32 dS' tile of this query tile: its own buffer, or (INPL) the
+      // tile's natural stage, which GEMM1/2 finished reading before s_full
+      const uint32_t dsn_tile =
+          dsn_lane + smem_u32(smem + (L::INPL ? L::OFF_Q + (t % NAT) * L::NAT_STRIDE
+                                              : L::OFF_DSN + pb * L::P_BYTES));
+      constexpr int CW = 16, NH = 1;  // columns per chunk
 #pragma unroll 1
-      for (int c0 = cbeg; c0 < cbeg + L::COLS; c0 += 16) {
-        uint32_t rs16[16], rd16[16];
-        tmem_ld16(t_s + c0, rs16);
-        tmem_ld16(t_dp + c0, rd16);
+      for (int ci = 0; ci < L::COLS / CW; ++ci) {
+        const int c0 = cbeg + ci * CW;
+        // the chunk's S^T and dP^T columns, all loads in flight at once
+        uint32_t rsA[NH][16], rdA[NH][16];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          tmem_ld16(t_s + c0 + hh * 16, rsA[hh]);
+          tmem_ld16(t_dp + c0 + hh * 16, rdA[hh]);
+        }
         tmem_ld_wait();
-        if (c0 + 16 == cbeg + L::COLS) {  // this warp's last read of the score buffer
+        if (!L::INPL && c0 + CW == cbeg + L::COLS) {  // last read of the score buffer
           tc_fence_before();
           mbar_arrive(&s_free[b]);
         }
-        float pm[16], ds[16];
+        float pmA[NH][16], dsA[NH][16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
-        if (j >= 0) {
-          if (!a.has_mask && !a.dropout) {
-            // two queries at a time with packed fp32x2 arithmetic
-            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c0);
-            const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
-            const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
-            const uint64_t sc2 = pk2(a.scale, a.scale);
+        for (int hh = 0; hh < NH; ++hh) {
+          const int c1 = c0 + hh * 16;  // first column of this 16-column half
+          const uint32_t(&rs16)[16] = rsA[hh];
+          const uint32_t(&rd16)[16] = rdA[hh];
+          float(&pm)[16] = pmA[hh];
+          float(&ds)[16] = dsA[hh];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
-                                           __uint_as_float(rs16[2 * i + 1])),
-                                       c2, nl2[i]);
-              float x0, x1;
-              up2(x, x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              const uint64_t d = f2mul(f2mul(pk2(p0, p1), sc2),
-                                       f2sub(pk2(__uint_as_float(rd16[2 * i]),
-                                                 __uint_as_float(rd16[2 * i + 1])),
-                                             dl2[i]));
-              pm[2 * i] = p0;
-              pm[2 * i + 1] = p1;
-              up2(d, ds[2 * i], ds[2 * i + 1]);
-            }
-            if (!plain) {
-              // tiles that straddle the causal diagonal, the window edge or the
-              // sequence ends: zero the pairs the visibility rule excludes
+          for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
+          if (j >= 0) {
+            if (!a.has_mask && !a.dropout) {
+              // two queries at a time with packed fp32x2 arithmetic
+              const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c1);
+              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c1);
+              const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
+              const uint64_t sc2 = pk2(a.scale, a.scale);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
+                                             __uint_as_float(rs16[2 * i + 1])),
+                                         c2, nl2[i]);
+                float x0, x1;
+                up2(x, x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                const uint64_t d = f2mul(f2mul(pk2(p0, p1), sc2),
+                                         f2sub(pk2(__uint_as_float(rd16[2 * i]),
+                                                   __uint_as_float(rd16[2 * i + 1])),
+                                               dl2[i]));
+                pm[2 * i] = p0;
+                pm[2 * i + 1] = p1;
+                up2(d, ds[2 * i], ds[2 * i + 1]);
+              }
+              if (!plain) {
+                // tiles that straddle the causal diagonal, the window edge or the
+                // sequence ends: zero the pairs the visibility rule excludes
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const int q = q0 + c1 + c;
+                  const int qa = q + (int)a.causal_offset;
+                  bool vis = (q < a.Sq) && key_ok;
+                  if (a.causal) vis = vis && (kj <= qa);
+                  if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
+                  pm[c] = vis ? pm[c] : 0.f;
+                  ds[c] = vis ? ds[c] : 0.f;
+                }
+              }
+            } else {
+              // additive mask and / or dropout: per-pair exponent addend
+              // (-inf for invisible or hard-masked pairs) and multiplier, then
+              // the same packed arithmetic as above
+              float add[16], mul[16];
+              uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
-                const int q = q0 + c0 + c;
+                const int q = q0 + c1 + c;
                 const int qa = q + (int)a.causal_offset;
                 bool vis = (q < a.Sq) && key_ok;
                 if (a.causal) vis = vis && (kj <= qa);
                 if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
-                pm[c] = vis ? pm[c] : 0.f;
-                ds[c] = vis ? ds[c] : 0.f;
-              }
-            }
-          } else {
-            // additive mask and / or dropout: per-pair exponent addend
-            // (-inf for invisible or hard-masked pairs) and multiplier, then
-            // the same packed arithmetic as above
-            float add[16], mul[16];
-            uint32_t words[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int q = q0 + c0 + c;
-              const int qa = q + (int)a.causal_offset;
-              bool vis = (q < a.Sq) && key_ok;
-              if (a.causal) vis = vis && (kj <= qa);
-              if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
-              float ad = sLSE[c0 + c];
-              if (a.has_mask && vis) {
-                const float m = __ldg(mrow + (long long)q * a.msq);
-                vis = m > -1.0e30f;
-                ad = fmaf(m, kLog2e, ad);
-              }
-              add[c] = vis ? ad : __int_as_float(0xff800000);
-              float mult = 1.f;
-              if (a.dropout) {
-                // one Philox call per 4 consecutive queries of this key
-                if ((c & 3) == 0) {
-                  const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u,
-                                                  a.seed_lo, a.seed_hi);
-                  words[0] = r.w[0];
-                  words[1] = r.w[1];
-                  words[2] = r.w[2];
-                  words[3] = r.w[3];
+                float ad = sLSE[c1 + c];
+                if (a.has_mask && vis) {
+                  const float m = __ldg(mrow + (long long)q * a.msq);
+                  vis = m > -1.0e30f;
+                  ad = fmaf(m, kLog2e, ad);
                 }
-                mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
+                add[c] = vis ? ad : __int_as_float(0xff800000);
+                float mult = 1.f;
+                if (a.dropout) {
+                  // one Philox call per 4 consecutive queries of this key
+                  if ((c & 3) == 0) {
+                    const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u,
+                                                    a.seed_lo, a.seed_hi);
+                    words[0] = r.w[0];
+                    words[1] = r.w[1];
+                    words[2] = r.w[2];
+                    words[3] = r.w[3];
+                  }
+                  mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
+                }
+                mul[c] = mult;
               }
-              mul[c] = mult;
-            }
-            const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
-            const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
-            const uint64_t sc2 = pk2(a.scale, a.scale);
+              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c1);
+              const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
+              const uint64_t sc2 = pk2(a.scale, a.scale);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
-                                           __uint_as_float(rs16[2 * i + 1])),
-                                       c2, pk2(add[2 * i], add[2 * i + 1]));
-              float x0, x1;
-              up2(x, x0, x1);
-              const uint64_t p2 = pk2(ex2_approx(x0), ex2_approx(x1));
-              const uint64_t m2 = pk2(mul[2 * i], mul[2 * i + 1]);
-              const uint64_t dp2 = f2mul(pk2(__uint_as_float(rd16[2 * i]),
-                                             __uint_as_float(rd16[2 * i + 1])),
-                                         m2);
-              const uint64_t d = f2mul(f2mul(p2, sc2), f2sub(dp2, dl2[i]));
-              up2(f2mul(p2, m2), pm[2 * i], pm[2 * i + 1]);
-              up2(d, ds[2 * i], ds[2 * i + 1]);
+              for (int i = 0; i < 8; ++i) {
+                const uint64_t x = f2fma(pk2(__uint_as_float(rs16[2 * i]),
+                                             __uint_as_float(rs16[2 * i + 1])),
+                                         c2, pk2(add[2 * i], add[2 * i + 1]));
+                float x0, x1;
+                up2(x, x0, x1);
+                const uint64_t p2 = pk2(ex2_approx(x0), ex2_approx(x1));
+                const uint64_t m2 = pk2(mul[2 * i], mul[2 * i + 1]);
+                const uint64_t dp2 = f2mul(pk2(__uint_as_float(rd16[2 * i]),
+                                               __uint_as_float(rd16[2 * i + 1])),
+                                           m2);
+                const uint64_t d = f2mul(f2mul(p2, sc2), f2sub(dp2, dl2[i]));
+                up2(f2mul(p2, m2), pm[2 * i], pm[2 * i + 1]);
+                up2(d, ds[2 * i], ds[2 * i + 1]);
+              }
             }
           }
         }
         // GEMM3-5 of tile t - PB must be done with this tile's P / dS' buffers
-        if (c0 == cbeg && t >= PB &&
+        // (in place: only the shared-memory dS' tile, waited for below)
+        if (!L::INPL && c0 == cbeg && t >= PB &&
             !warp_wait(&mma5_par[pb], ((t / PB) - 1) & 1, a.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // P^T (and, for fp32, dS'^T) into tensor memory: the A operands of
-        // GEMM3 / GEMM4.  Whole warps: tcgen05.st is warp-collective.
-        if constexpr (BF16) {
-          uint32_t pk[8];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) pk[c] = pack_bf16(pm[2 * c], pm[2 * c + 1]);
-          tmem_st8(t_p + c0 / 2, pk);
-        } else {
-          uint32_t pr[16], dr[16];
+        for (int hh = 0; hh < NH; ++hh) {
+          const int c1 = c0 + hh * 16;
+          const float(&pm)[16] = pmA[hh];
+          const float(&ds)[16] = dsA[hh];
+          // P^T (and, for fp32, dS'^T) into tensor memory: the A operands of
+          // GEMM3 / GEMM4.  Whole warps: tcgen05.st is warp-collective.
+          if constexpr (BF16) {
+            uint32_t pk[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            pr[c] = to_tf32(pm[c]);
-            dr[c] = to_tf32(ds[c]);
+            for (int c = 0; c < 8; ++c) pk[c] = pack_bf16(pm[2 * c], pm[2 * c + 1]);
+            tmem_st8(t_p + c1 / 2, pk);
+          } else {
+            uint32_t pr[16], dr[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              pr[c] = to_tf32(pm[c]);
+              dr[c] = to_tf32(ds[c]);
+            }
+            tmem_st16(t_p + c1, pr);
+            tmem_st16(t_ds + c1, dr);
+            if (j >= 0) {
+              // dS' as [BM rows (queries)][BN keys] for GEMM5's K-major operand
+              const uint32_t rowbase = dsn_tile + c1 * 128;
+#pragma unroll
+              for (int c = 0; c < 16; ++c) st_shared_b32(rowbase + c * 128 + xo[c & 7], dr[c]);
+            }
           }
-          tmem_st16(t_p + c0, pr);
-          tmem_st16(t_ds + c0, dr);
-          if (j >= 0) {
-            // dS' as [BM rows (queries)][BN keys] for GEMM5's K-major operand
-            const uint32_t rowbase = dsn_lane + pb * L::P_BYTES + c0 * 128;
+          if constexpr (BF16) {
+            if (j >= 0) {
+              // dS'^T [BN rows][BM]: GEMM4's A and GEMM5's operand
+              const int blk = c1 / W;
+              const int pos = (c1 % W) * E;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) st_shared_b32(rowbase + c * 128 + xo[c & 7], dr[c]);
-          }
-        }
-        if constexpr (BF16) {
-          if (j >= 0) {
-            // dS'^T [BN rows][BM]: GEMM4's A and GEMM5's operand
-            const int blk = c0 / W;
-            const int pos = (c0 % W) * E;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
-              st_shared_v4(smem_u32(sdS + off), pack_bf16(ds[h2 * 8 + 0], ds[h2 * 8 + 1]),
-                           pack_bf16(ds[h2 * 8 + 2], ds[h2 * 8 + 3]),
-                           pack_bf16(ds[h2 * 8 + 4], ds[h2 * 8 + 5]),
-                           pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
+                st_shared_v4(smem_u32(sdS + off), pack_bf16(ds[h2 * 8 + 0], ds[h2 * 8 + 1]),
+                             pack_bf16(ds[h2 * 8 + 2], ds[h2 * 8 + 3]),
+                             pack_bf16(ds[h2 * 8 + 4], ds[h2 * 8 + 5]),
+                             pack_bf16(ds[h2 * 8 + 6], ds[h2 * 8 + 7]));
+              }
             }
           }
         }
