@@ -26,12 +26,18 @@
 //    (GEMM3/4) travel in separate rings, so a natural stage is released as
 //    soon as GEMM1/2 are done with it.
 //
-// Pipeline.  GEMM1/2 of tile t + NSB are issued as soon as the softmax warps
-// have read tile t's scores out of tensor memory (NSB = 1 or 2 score
-// buffers), then GEMM3-5 of tile t once its P / dS' are written; the softmax
-// warps compute tile t while the tensor cores finish earlier tiles and start
-// later ones, and only wait for GEMM3-5 of tile t - PB (PB = 1 or 2 P / dS'
-// buffers) before overwriting P / dS'.
+// Pipeline.  GEMM1/2 of tile t + NSB are issued as soon as score buffer
+// t % NSB is free (NSB = 1 or 2 score buffers), then GEMM3-5 of tile t once
+// its P / dS' are written; the softmax warps compute tile t while the tensor
+// cores finish earlier tiles and start later ones.  With separate P / dS'
+// columns a score buffer is free once the softmax warps have read it, and
+// they wait for GEMM3-5 of tile t - PB (PB = 1 or 2 P / dS' buffers) before
+// overwriting P / dS'.  In place (fp32, D = 64) a score buffer is free only
+// after GEMM3/4 have read the P / dS' written over it: GEMM3/4 (t), GEMM5 (t),
+// then GEMM1/2 (t + 2) once GEMM3/4 (t) are complete.  The tensor cores read operands from shared memory at
+// up to 128 bytes per clock; while they do, other shared-memory traffic
+// (including mbarrier operations) is served slowly, so the fp32 softmax reads
+// per-query LSE / Delta once per tile in 16x256b fragments.
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer: resident key tiles, natural Q / dO ring
@@ -301,6 +307,92 @@ __device__ __forceinline__ bool tile_is_plain(const TileArgs& a, int q0, int BM,
   return true;
 }
 
+// fp32 in-place softmax step in 16x256b fragments, for tiles without an
+// additive mask or dropout.  A softmax warp covers the 32 key rows of its TMEM
+// sub-partition and a 32-column share of the query tile; thread t owns key
+// rows t/4 + 8k (k < 4) and query columns 8x + 2(t%4) + e (x < 4, e < 2), so
+// it needs -LSE*log2e and Delta of only 8 queries, loaded once per tile (the
+// per-column broadcast loads of a one-key-per-thread layout queue behind the
+// tensor cores' shared-memory operand reads).  Writes P (TF32) over S^T and
+// dS' over dP^T, and dS' into the swizzled [query rows][keys] tile.
+//   t_s, t_dp   tensor-memory address of the share (sub-partition lane base,
+//               first column of the share)
+//   sNL, sDelta the share's first query in the LSE2 / Delta rows
+//   q0, k0      first query of the share, first key of the sub-partition
+//   dsn         this thread's base address in the dS' tile (see the caller)
+//   xo2         swizzle term of key group k and column parity e, [2k + e]
+__device__ __forceinline__ void softmax_frag(const TileArgs& a, uint32_t t_s, uint32_t t_dp,
+                                             const float* sNL, const float* sDelta, bool plain,
+                                             int q0, int k0, bool (&key_ok)[4], uint32_t dsn,
+                                             const uint32_t (&xo2)[8]) {
+  const int lane = threadIdx.x & 31, tq = lane & 3, tr = lane >> 2;
+  uint64_t nl2[4], dl2[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    nl2[x] = *reinterpret_cast<const uint64_t*>(sNL + 8 * x + 2 * tq);
+    dl2[x] = *reinterpret_cast<const uint64_t*>(sDelta + 8 * x + 2 * tq);
+  }
+  const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
+  const uint64_t sc2 = pk2(a.scale, a.scale);
+#pragma unroll
+  for (int lb = 0; lb < 2; ++lb) {  // lanes 0-15, then 16-31 of the sub-partition
+    uint32_t sv[16], dv[16];
+    tmem_ld_16x256b_x4(t_s + ((uint32_t)(16 * lb) << 16), sv);
+    tmem_ld_16x256b_x4(t_dp + ((uint32_t)(16 * lb) << 16), dv);
+    tmem_ld_wait();
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = 4 * x + 2 * r;
+        const uint64_t xx = f2fma(pk2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2,
+                                  nl2[x]);
+        float x0, x1;
+        up2(xx, x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const uint64_t d = f2mul(
+            f2mul(pk2(p0, p1), sc2),
+            f2sub(pk2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), dl2[x]));
+        float d0, d1;
+        up2(d, d0, d1);
+        sv[i] = __float_as_uint(p0);
+        sv[i + 1] = __float_as_uint(p1);
+        dv[i] = __float_as_uint(d0);
+        dv[i + 1] = __float_as_uint(d1);
+      }
+    }
+    if (!plain) {
+      // tiles that straddle the causal diagonal, the window edge or the
+      // sequence ends: zero the pairs the visibility rule excludes
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int kk = 2 * lb + ((i >> 1) & 1);  // key group of register i
+        const int kj = k0 + tr + 8 * kk;
+        const int q = q0 + 8 * (i >> 2) + 2 * tq + (i & 1);
+        const int qa = q + (int)a.causal_offset;
+        bool vis = (q < a.Sq) && key_ok[kk];
+        if (a.causal) vis = vis && (kj <= qa);
+        if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
+        sv[i] = vis ? sv[i] : 0u;
+        dv[i] = vis ? dv[i] : 0u;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      sv[i] = to_tf32(__uint_as_float(sv[i]));
+      dv[i] = to_tf32(__uint_as_float(dv[i]));
+    }
+    tmem_st_16x256b_x4(t_s + ((uint32_t)(16 * lb) << 16), sv);
+    tmem_st_16x256b_x4(t_dp + ((uint32_t)(16 * lb) << 16), dv);
+    // dS' tile: query row 8x + 2(t%4) + e of the share, key group 2 lb + r
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int x = i >> 2, r = (i >> 1) & 1, e = i & 1;
+      st_shared_b32(dsn + (8 * x + e) * 128 + xo2[2 * (2 * lb + r) + e], dv[i]);
+    }
+  }
+}
+
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -524,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (L::KMAJ && !L::INPL) mma_commit(&nat_empty[s]);
         return true;
       };
-      auto issue_back = [&](int t) -> bool {  // GEMM3, GEMM4, GEMM5 of tile t
+      auto issue_back34 = [&](int t) -> bool {  // GEMM3, GEMM4 of tile t
         if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, a.err)) return false;
         const int s = t % NAT, r = L::KMAJ ? t % TR : 0, pb = t % PB, b = t % NSB;
         // P^T and (fp32) dS'^T: A operands of GEMM3/4 in tensor memory
@@ -558,6 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (L::INPL) mma_commit(&pfree[b]);  // score buffer b reusable
         if constexpr (L::KMAJ) mma_commit(&tr_empty[r]);  // GEMM5 does not read them
+        return true;
+      };
+      auto issue_g5 = [&](int t) -> bool {  // GEMM5 of tile t
+        const int s = t % NAT, pb = t % PB;
         if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
         tc_fence_after();
 #pragma unroll
@@ -584,7 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // GEMM1/2 run NSB tiles ahead of GEMM3-5: front(t + NSB) only needs the
       // softmax warps to have read tile t's scores (s_free), which happens
       // before they finish tile t (p_full), so the tensor cores compute the
-      // next scores while the softmax warps are still busy.
+      // next scores while the softmax warps are still busy.  In place, score
+      // buffer t % NSB cycles through GEMM1/2 (t), the softmax warps and
+      // GEMM3/4 (t) before GEMM1/2 (t + NSB) may rewrite it; GEMM5 (t) runs
+      // while the issuer waits for GEMM3/4 (t) to complete.
       if constexpr (L::VTM) {
         ok = ok && mbar_wait(v_ready, 0, a.err);
         tc_fence_after();
@@ -593,13 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!issue_front(t)) ok = false;
       for (int t = 0; ok && t < T; ++t) {
         if constexpr (L::INPL) {
-          // in place: buffer t % NSB is rewritten only after GEMM3/4 of tile t
-          // read it; GEMM5 of tile t keeps the tensor cores busy meanwhile
-          if (!issue_back(t)) { ok = false; break; }
-          if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
+          ok = issue_back34(t) && issue_g5(t) && (t + NSB >= T || issue_front(t + NSB));
         } else {
-          if (t + NSB < T && !issue_front(t + NSB)) { ok = false; break; }
-          if (!issue_back(t)) { ok = false; break; }
+          ok = (t + NSB >= T || issue_front(t + NSB)) && issue_back34(t) && issue_g5(t);
         }
       }
       if (ok) mma_commit(acc_done);
@@ -622,6 +717,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t xo[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) xo[k] = (uint32_t)(((((jj % W) * 4) >> 4) ^ k) << 4);
+    // fp32 in-place tiles without mask / dropout use 16x256b fragments (see
+    // softmax_frag): this thread's key rows, its offset in the dS' tile and the
+    // swizzle term of each (key group, column parity)
+    const int tq = lane & 3, tr = lane >> 2;
+    bool key_ok4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) key_ok4[k] = w.k0 + quad * 32 + tr + 8 * k < a.Sk;
+    const uint32_t dsn_frag = quad * BM * 128 + (cbeg + 2 * tq) * 128 + (tr % 4) * 4;
+    uint32_t xo2[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) xo2[2 * k + e] = (uint32_t)((((tr / 4 + 2 * k) ^ (2 * tq + e))) << 4);
     bool ok = true;
     if constexpr (L::VTM) {
       if (T > 0) {
@@ -675,40 +783,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_ds = L::INPL ? t_dp : tmem + lane_base + L::T_DS + pb * BM;
       // fp32 dS' tile of this query tile: its own buffer, or (INPL) the
       // tile's natural stage, which GEMM1/2 finished reading before s_full
-      const uint32_t dsn_tile =
-          dsn_lane + smem_u32(smem + (L::INPL ? L::OFF_Q + (t % NAT) * L::NAT_STRIDE
-                                              : L::OFF_DSN + pb * L::P_BYTES));
-      constexpr int CW = 16, NH = 1;  // columns per chunk
+      const uint32_t dsn_base = smem_u32(
+          smem + (L::INPL ? L::OFF_Q + (t % NAT) * L::NAT_STRIDE : L::OFF_DSN + pb * L::P_BYTES));
+      const uint32_t dsn_tile = dsn_lane + dsn_base;
+      if (L::INPL && !a.has_mask && !a.dropout) {
+        softmax_frag(a, t_s + cbeg, t_dp + cbeg, sLSE + cbeg, sDelta + cbeg, plain, q0 + cbeg,
+                     w.k0 + quad * 32, key_ok4, dsn_base + dsn_frag, xo2);
+      } else {
 #pragma unroll 1
-      for (int ci = 0; ci < L::COLS / CW; ++ci) {
-        const int c0 = cbeg + ci * CW;
-        // the chunk's S^T and dP^T columns, all loads in flight at once
-        uint32_t rsA[NH][16], rdA[NH][16];
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-          tmem_ld16(t_s + c0 + hh * 16, rsA[hh]);
-          tmem_ld16(t_dp + c0 + hh * 16, rdA[hh]);
-        }
-        tmem_ld_wait();
-        if (!L::INPL && c0 + CW == cbeg + L::COLS) {  // last read of the score buffer
-          tc_fence_before();
-          mbar_arrive(&s_free[b]);
-        }
-        float pmA[NH][16], dsA[NH][16];
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-          const int c1 = c0 + hh * 16;  // first column of this 16-column half
-          const uint32_t(&rs16)[16] = rsA[hh];
-          const uint32_t(&rd16)[16] = rdA[hh];
-          float(&pm)[16] = pmA[hh];
-          float(&ds)[16] = dsA[hh];
+        for (int c0 = cbeg; c0 < cbeg + L::COLS; c0 += 16) {
+          uint32_t rs16[16], rd16[16];
+          tmem_ld16(t_s + c0, rs16);
+          tmem_ld16(t_dp + c0, rd16);
+          tmem_ld_wait();
+          if (!L::INPL && c0 + 16 == cbeg + L::COLS) {  // last read of the score buffer
+            tc_fence_before();
+            mbar_arrive(&s_free[b]);
+          }
+          float pm[16], ds[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) pm[c] = ds[c] = 0.f;
           if (j >= 0) {
             if (!a.has_mask && !a.dropout) {
               // two queries at a time with packed fp32x2 arithmetic
-              const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c1);
-              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c1);
+              const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c0);
+              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
               const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
               const uint64_t sc2 = pk2(a.scale, a.scale);
 #pragma unroll
@@ -732,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // sequence ends: zero the pairs the visibility rule excludes
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                  const int q = q0 + c1 + c;
+                  const int q = q0 + c0 + c;
                   const int qa = q + (int)a.causal_offset;
                   bool vis = (q < a.Sq) && key_ok;
                   if (a.causal) vis = vis && (kj <= qa);
@@ -749,12 +848,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
-                const int q = q0 + c1 + c;
+                const int q = q0 + c0 + c;
                 const int qa = q + (int)a.causal_offset;
                 bool vis = (q < a.Sq) && key_ok;
                 if (a.causal) vis = vis && (kj <= qa);
                 if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
-                float ad = sLSE[c1 + c];
+                float ad = sLSE[c0 + c];
                 if (a.has_mask && vis) {
                   const float m = __ldg(mrow + (long long)q * a.msq);
                   vis = m > -1.0e30f;
@@ -776,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mul[c] = mult;
               }
-              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c1);
+              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
               const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
               const uint64_t sc2 = pk2(a.scale, a.scale);
 #pragma unroll
@@ -797,27 +896,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-        }
-        // GEMM3-5 of tile t - PB must be done with this tile's P / dS' buffers
-        // (in place: only the shared-memory dS' tile, waited for below)
-        if (!L::INPL && c0 == cbeg && t >= PB &&
-            !warp_wait(&mma5_par[pb], ((t / PB) - 1) & 1, a.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-          const int c1 = c0 + hh * 16;
-          const float(&pm)[16] = pmA[hh];
-          const float(&ds)[16] = dsA[hh];
+          // GEMM3-5 of tile t - PB must be done with this tile's P / dS' buffers
+          // (in place: only the shared-memory dS' tile, waited for below)
+          if (!L::INPL && c0 == cbeg && t >= PB &&
+              !warp_wait(&mma5_par[pb], ((t / PB) - 1) & 1, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           // P^T (and, for fp32, dS'^T) into tensor memory: the A operands of
           // GEMM3 / GEMM4.  Whole warps: tcgen05.st is warp-collective.
           if constexpr (BF16) {
             uint32_t pk[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) pk[c] = pack_bf16(pm[2 * c], pm[2 * c + 1]);
-            tmem_st8(t_p + c1 / 2, pk);
+            tmem_st8(t_p + c0 / 2, pk);
           } else {
             uint32_t pr[16], dr[16];
 #pragma unroll
@@ -825,11 +918,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               pr[c] = to_tf32(pm[c]);
               dr[c] = to_tf32(ds[c]);
             }
-            tmem_st16(t_p + c1, pr);
-            tmem_st16(t_ds + c1, dr);
+            tmem_st16(t_p + c0, pr);
+            tmem_st16(t_ds + c0, dr);
             if (j >= 0) {
               // dS' as [BM rows (queries)][BN keys] for GEMM5's K-major operand
-              const uint32_t rowbase = dsn_tile + c1 * 128;
+              const uint32_t rowbase = dsn_tile + c0 * 128;
 #pragma unroll
               for (int c = 0; c < 16; ++c) st_shared_b32(rowbase + c * 128 + xo[c & 7], dr[c]);
             }
@@ -837,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (BF16) {
             if (j >= 0) {
               // dS'^T [BN rows][BM]: GEMM4's A and GEMM5's operand
-              const int blk = c1 / W;
-              const int pos = (c1 % W) * E;
+              const int blk = c0 / W;
+              const int pos = (c0 % W) * E;
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
                 const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
