@@ -337,6 +337,7 @@ __device__ __forceinline__ void softmax_frag(const TileArgs& a, uint32_t t_s, ui
 #pragma unroll
   for (int lb = 0; lb < 2; ++lb) {  // lanes 0-15, then 16-31 of the sub-partition
     uint32_t sv[16], dv[16];
+    __syncwarp();  // tcgen05.ld / st are warp-collective
     tmem_ld_16x256b_x4(t_s + ((uint32_t)(16 * lb) << 16), sv);
     tmem_ld_16x256b_x4(t_dp + ((uint32_t)(16 * lb) << 16), dv);
     tmem_ld_wait();
@@ -382,6 +383,7 @@ __device__ __forceinline__ void softmax_frag(const TileArgs& a, uint32_t t_s, ui
       sv[i] = to_tf32(__uint_as_float(sv[i]));
       dv[i] = to_tf32(__uint_as_float(dv[i]));
     }
+    __syncwarp();
     tmem_st_16x256b_x4(t_s + ((uint32_t)(16 * lb) << 16), sv);
     tmem_st_16x256b_x4(t_dp + ((uint32_t)(16 * lb) << 16), dv);
     // dS' tile: query row 8x + 2(t%4) + e of the share, key group 2 lb + r
@@ -793,6 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c0 = cbeg; c0 < cbeg + L::COLS; c0 += 16) {
           uint32_t rs16[16], rd16[16];
+          __syncwarp();  // tcgen05.ld / st are warp-collective; the math below diverges on j
           tmem_ld16(t_s + c0, rs16);
           tmem_ld16(t_dp + c0, rd16);
           tmem_ld_wait();
@@ -904,6 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          __syncwarp();
           // P^T (and, for fp32, dS'^T) into tensor memory: the A operands of
           // GEMM3 / GEMM4.  Whole warps: tcgen05.st is warp-collective.
           if constexpr (BF16) {
@@ -963,7 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c0 = half * DH; c0 < (half + 1) * DH; c0 += 16) {
         uint32_t rv[16], rk[16];
-        if (have) {  // whole warps: tcgen05.ld is warp-collective
+        __syncwarp();  // the stores below diverge on key_ok; tcgen05.ld is warp-collective
+        if (have) {
           tmem_ld16(tmem + lane_base + L::T_DV + c0, rv);
           tmem_ld16(tmem + lane_base + L::T_DK + c0, rk);
           tmem_ld_wait();
@@ -971,8 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) rv[c] = rk[c] = 0u;
         }
-        if (!key_ok) continue;
-        if constexpr (BF16) {
+        if (!key_ok) {
+          // key past the end of the sequence: nothing to store
+        } else if constexpr (BF16) {
           uint4* dv = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dV) + off + c0);
           uint4* dk = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dK) + off + c0);
 #pragma unroll
@@ -1018,6 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every dQ thread is also done reading the staging tile of tile t-1
       if (!dq_group_all(mbar_wait(mma5_done, t & 1, a.err))) break;
       tc_fence_after();
+      __syncwarp();  // tcgen05.ld is warp-collective; the staging below diverges on r
       float v[L::N5];
 #pragma unroll
       for (int c0 = 0; c0 < L::N5; c0 += 16) {
