@@ -778,8 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + rs * BM * 4);
       const uint32_t bh = (uint32_t)(w.b * a.H + h);
       const bool plain = tile_is_plain(a, q0, BM, w.k0, BN);
-      const float* mrow = a.has_mask ? a.mask + w.b * a.msb + h * a.msh + (long long)kj * a.msk
-                                     : nullptr;
       const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
       const uint32_t t_p = L::INPL ? t_s : tmem + lane_base + L::T_P + pb * L::PCOLS;
       const uint32_t t_ds = L::INPL ? t_dp : tmem + lane_base + L::T_DS + pb * BM;
@@ -846,9 +844,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               // additive mask and / or dropout: per-pair exponent addend
               // (-inf for invisible or hard-masked pairs) and multiplier, then
-              // the same packed arithmetic as above
+              // the same packed arithmetic as above.  The chunk's four Philox
+              // calls (one per four consecutive queries of this key) become a
+              // 16-bit keep mask first, and its 16 mask values are loaded
+              // together from in-range addresses, so the loads overlap.
+              uint32_t keep_bits = 0xffffu;
+              if (a.dropout) {
+                keep_bits = 0u;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                  const Philox4 r = philox4x32_10((uint32_t)(q0 + c0 + 4 * g4) >> 2, (uint32_t)kj,
+                                                  bh, 0u, a.seed_lo, a.seed_hi);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    keep_bits |= (r.w[e] >= a.drop_threshold ? 1u : 0u) << (4 * g4 + e);
+                }
+              }
+              float mv[16];
+              if (a.has_mask) {
+                const float* mr = a.mask + w.b * a.msb + h * a.msh +
+                                  (long long)(kj < a.Sk ? kj : a.Sk - 1) * a.msk;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const int q = q0 + c0 + c < a.Sq ? q0 + c0 + c : a.Sq - 1;
+                  mv[c] = __ldg(mr + (long long)q * a.msq);
+                }
+              }
               float add[16], mul[16];
-              uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
                 const int q = q0 + c0 + c;
@@ -857,26 +879,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (a.causal) vis = vis && (kj <= qa);
                 if (a.window > 0) vis = vis && (abs(qa - kj) < (int)a.window);
                 float ad = sLSE[c0 + c];
-                if (a.has_mask && vis) {
-                  const float m = __ldg(mrow + (long long)q * a.msq);
-                  vis = m > -1.0e30f;
-                  ad = fmaf(m, kLog2e, ad);
+                if (a.has_mask) {
+                  vis = vis && mv[c] > -1.0e30f;
+                  ad = fmaf(mv[c], kLog2e, ad);
                 }
                 add[c] = vis ? ad : __int_as_float(0xff800000);
-                float mult = 1.f;
-                if (a.dropout) {
-                  // one Philox call per 4 consecutive queries of this key
-                  if ((c & 3) == 0) {
-                    const Philox4 r = philox4x32_10((uint32_t)q >> 2, (uint32_t)kj, bh, 0u,
-                                                    a.seed_lo, a.seed_hi);
-                    words[0] = r.w[0];
-                    words[1] = r.w[1];
-                    words[2] = r.w[2];
-                    words[3] = r.w[3];
-                  }
-                  mult = words[c & 3] >= a.drop_threshold ? a.drop_inv_keep : 0.f;
-                }
-                mul[c] = mult;
+                mul[c] = ((keep_bits >> c) & 1u) ? (a.dropout ? a.drop_inv_keep : 1.f) : 0.f;
               }
               const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
               const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
