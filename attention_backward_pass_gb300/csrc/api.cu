@@ -167,6 +167,31 @@ CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int
 
 }  // namespace
 
+// Dense fp32 tensor of `rank` dimensions (dims[0] innermost and contiguous,
+// each further dimension packed after the previous; base and dims[0] * 4
+// 16-byte aligned), copied in boxes of box[] elements, plain or with the
+// 128-byte swizzle.  Elements outside the tensor read as zero and are not
+// written.
+CUresult make_f32_map(CUtensorMap* m, const void* base, int rank, const long long* dims,
+                      const int* box, bool swizzle128) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rank < 1 || rank > 5) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  unsigned long long stride = 4;
+  for (int i = 0; i < rank; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    bx[i] = (cuuint32_t)box[i];
+    es[i] = 1;
+    stride *= (unsigned long long)dims[i];
+    if (i + 1 < rank) st[i] = (cuuint64_t)stride;
+  }
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), d, st,
+             bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 unsigned int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

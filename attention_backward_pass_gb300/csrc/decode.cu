@@ -2,24 +2,42 @@
 //
 // The decode page ("rullama attention_backward_dq.wgsl") runs one workgroup
 // per query head and sweeps the K/V history three times (d_probs, d_scores,
-// then d_q with a strided, uncoalesced k_hist walk).  Here the history of a
-// (sequence, KV head) is read from HBM exactly once for all the query heads
-// that share it, using
-//   d_q_h = sum_j probs_hj (dp_hj - sum_pd_h) k_j
-//         = sum_j probs_hj dp_hj k_j  -  sum_pd_h * sum_j probs_hj k_j,
-// so one pass over the history can accumulate both sums together with
-// sum_pd_h = sum_j probs_hj dp_hj, and a small finalize kernel combines them.
+// then d_q with a strided, uncoalesced k_hist walk).  Here each history
+// tensor is read from HBM exactly once for all the G query heads that share
+// a KV head, in two passes split at sum_pd_h = sum_j probs_hj dp_hj:
+//   decode_dp (reads V):  dp_hj = d_out_h . v_j; parks probs_hj dp_hj in
+//                         d_scores; per-CTA partial sums of sum_pd_h
+//   decode_dq (reads K):  d_scores_hj = probs_hj dp_hj - probs_hj sum_pd_h
+//                         (final values), d_q_h = sum_j d_scores_hj k_j
+// The split costs one extra read of the parked values (G floats per key,
+// next to the 2 D floats of K and V).  A single pass would need two d_q
+// accumulators instead (sum_j probs dp k_j and sum_j probs k_j, combined
+// once sum_pd is known): 2 G D multiply-adds per key in place of G D.
 //
-// decode_main: grid (splits, seqs * n_kv).  Each CTA streams its share of the
-//   history in chunks of CH keys, double-buffered in shared memory with bulk
-//   async copies.  Phase 1 (warp per key): dp_hj = d_out_h . v_j for all G
-//   heads, lane-split over d and reduced with a transposing butterfly; dp is
-//   parked in d_scores.  Phase 2 (thread per d): accumulate
-//   A_h[d] += probs_hj dp_hj k_j[d] and B_h[d] += probs_hj k_j[d].
-//   Per-CTA partials (sum_pd, A, B) go to the workspace.
-// decode_finalize: grid (n_heads, seqs).  Sums the partials, writes
-//   d_q = A - sum_pd B, and rewrites d_scores = probs (dp - sum_pd).
+// Both kernels run one CTA per SM.  The (sequence, KV head) x chunk space
+// (chunks of CH keys) is split evenly over the CTAs, identically in both
+// passes, so a CTA's range covers one or a few (sequence, KV head) pairs
+// ("segments").  A producer warp streams each chunk's K or V rows (one 4-D
+// tensor copy) through a ring of NS shared-memory stages, and -- when the
+// history length is a multiple of 4 -- the chunk's [G][CH] slices of probs /
+// d_scores with one 3-D tensor copy each; the compute warps meet it on
+// mbarriers.
+//   decode_dp compute warps: lane-split over d (D/32 per lane, d_out held in
+//     registers); key groups of warps take interleaved keys of every chunk.
+//     Each lane keeps its heads' d_out in an order permuted by its lane bits
+//     so that the warp reduction of the G per-key sums is a chain of plain
+//     shuffle-adds (no selects); one lane per head ends with the head's dp.
+//     probs*dp goes to a staging array of the stage, which the producer
+//     writes back with one tensor store when it recycles the stage.
+//   decode_dq compute threads: two d per thread, KG2 key groups.  Per chunk
+//     the threads first form the chunk's G x CH d_scores (coalesced stores,
+//     a copy kept in shared memory), then accumulate d_q.  The partial d_q of
+//     a segment goes to the workspace; the last CTA of a pair to finish (a
+//     counter in the workspace, zeroed by decode_dp) sums the partials in CTA
+//     order and writes d_q, so the result does not depend on timing.
 #include <cuda_runtime.h>
+
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -28,11 +46,8 @@ namespace attnbwd {
 
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kDecChunk = 16;     // keys per pipeline stage
-constexpr int kDecStages = 3;     // 3 stages x (K + V) x 16 rows x 1 KB = 96 KB at D = 256
-constexpr int kDecCtasPerSm = 2;
-constexpr int kDecSlots = 152 * kDecCtasPerSm;
+constexpr int kDecChunk = 32;                 // keys per chunk
+constexpr int kDecSmsFallback = 152;
 
 struct DecArgs {
   const float* k;
@@ -41,8 +56,16 @@ struct DecArgs {
   const float* d_out;
   float* d_scores;
   float* d_q;
-  float* partials;
-  int n_heads, n_kv, D, hist, n_split, keys_per_split;
+  float* part1;          // decode_dp: partial sum_pd   [grid][max_seg][SLOT1]
+  float* part2;          // decode_dq: partial d_q      [grid][max_seg][SLOT2]
+  unsigned int* count;   // per (sequence, KV head) pair: decode_dq CTAs done
+  int n_heads, n_kv, D, hist;
+  int grid;              // CTAs of either kernel
+  int cpp;               // chunks per (sequence, KV head) pair
+  int n_pairs;
+  long long n_chunks;
+  int max_seg;           // partial slots per CTA
+  int side_tma;          // [G][CH] slices of probs / d_scores move by tensor copies
   unsigned int* err;
 };
 
@@ -58,6 +81,39 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
+}
+
+// N consecutive floats (N = 2 or a multiple of 4) from a 4N-byte aligned address.
+template <int N>
+__device__ __forceinline__ void load_vec(float (&dst)[N], const float* src) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < N; k += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src + k);
+      dst[k] = t.x, dst[k + 1] = t.y, dst[k + 2] = t.z, dst[k + 3] = t.w;
+    }
+  } else {
+    static_assert(N == 2, "load_vec width");
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    dst[0] = t.x, dst[1] = t.y;
+  }
+}
+
+// bar.red.or over the `threads` threads of named barrier `id`.
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Sum G per-lane values over the warp so that the lanes of head g =
@@ -88,307 +144,583 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&x)[G], int lane) {
   return r;
 }
 
+// Chunk range [f0, f1) of CTA i; the CTA that owns chunk f.
+__host__ __device__ __forceinline__ long long dec_begin(long long i, long long n, int grid) {
+  return i * n / grid;
+}
+__host__ __device__ __forceinline__ int dec_cta_of(long long f, long long n, int grid) {
+  return (int)(((f + 1) * grid + n - 1) / n - 1);
+}
+
+constexpr int kDecSmemMax = 227 * 1024;  // dynamic + static shared memory of one CTA
+
+__host__ __device__ constexpr int dec_clamp(int x, int lo, int hi) { return x < lo ? lo : x > hi ? hi : x; }
+__host__ __device__ constexpr int dec_round(int x, int m) { return (x + m - 1) / m * m; }
+
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, (G * D / 32 <= 64) ? kDecCtasPerSm : 1)
-    decode_main_kernel(const DecArgs a) {
-  constexpr int DPL = D / 32;               // d values per lane in phase 1
-  constexpr int NKG = kDecThreads / D;      // key groups in phase 2
-  constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : 4;
-  constexpr int ROW_BYTES = D * 4;
-  constexpr int STAGE_BYTES = 2 * kDecChunk * ROW_BYTES;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  float* stage_base = reinterpret_cast<float*>(smem_raw);  // [stages][K|V][CH][D]
-  // key-major so that one vector load returns consecutive heads of a key
-  __shared__ __align__(16) float w1_s[kDecChunk][G];     // probs * dp
-  __shared__ __align__(16) float pr_s[2][kDecChunk][G];  // probs (chunk parity)
-  __shared__ float red_s[NKG > 1 ? NKG : 1][2 * G][NKG > 1 ? D : 1];  // only used if NKG > 1
-  __shared__ float sumpd_s[kDecThreads / 32][G];
-  __shared__ __align__(8) uint64_t full[kDecStages];
+struct DecCfg {
+  static constexpr int CH = kDecChunk;                    // keys per chunk
+  static constexpr int SIDE = G * CH;                     // floats of one [G][CH] side array
+  static constexpr int ROWS_BYTES = CH * D * 4;           // the chunk's K or V rows
+  static constexpr int STAGE = dec_round(ROWS_BYTES + 2 * SIDE * 4, 128);
+  // decode_dp: stage = [V rows [CH][D] | probs [G][CH] | probs*dp [G][CH]]
+  static constexpr int DPL = D / 32;                          // d per lane
+  static constexpr int HPW = G * DPL <= 64 ? G : 64 / DPL;    // heads per warp
+  static constexpr int LOG_HPW = HPW == 1 ? 0 : HPW == 2 ? 1 : HPW == 4 ? 2 : HPW == 8 ? 3 : 4;
+  static constexpr int NHG = G / HPW;                         // head groups
+  static constexpr int P1W = 8;                               // compute warps
+  static constexpr int KG = P1W / NHG;                        // key groups
+  static constexpr int NS1 = dec_clamp((kDecSmemMax - 2048) / STAGE, 2, 12);
+  static constexpr int SMEM1 = NS1 * STAGE + 128;             // + alignment slack
+  static constexpr int SLOT1 = KG * G;                        // sum_pd[KG][G]
+  // decode_dq: stage = [K rows [CH][D] | parked probs*dp | probs]
+  static constexpr int P2T = 256;                         // compute threads
+  static constexpr int KG2 = P2T * 2 / D;                 // key groups (two d per thread)
+  static constexpr int NS2 = dec_clamp((kDecSmemMax - 2048 - (2 * CH * G + G) * 4) / STAGE, 2, 12);
+  static constexpr int SMEM2 = NS2 * STAGE + 128;
+  static constexpr int SLOT2 = KG2 * G * D;               // d_q[KG2][G][D]
+  static_assert(HPW * DPL <= 64 && G % HPW == 0 && KG >= 1 && CH % KG == 0 && D % 64 == 0 &&
+                    D <= 256, "decode_dp split");
+  static_assert(KG2 >= 1 && CH % KG2 == 0, "decode_dq split");
+  static_assert(SMEM1 + 1024 <= kDecSmemMax && SMEM2 + (2 * CH * G + G) * 4 + 1024 <= kDecSmemMax,
+                "decode shared memory");
+};
 
-  const int split = blockIdx.x;
-  const int pair = blockIdx.y;  // seq * n_kv + kv
-  const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+// DPL = D / 32 values of a row for this lane: 16-byte pieces at 4 lane + 128 q
+// (q < DPL / 4), or 8 bytes at 2 lane when DPL = 2, so that a warp's loads
+// cover contiguous 512- / 256-byte runs.
+template <int DPL>
+__device__ __forceinline__ void load_lane(float (&dst)[DPL], const float* row, int lane) {
+  if constexpr (DPL % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < DPL / 4; ++q) {
+      const float4 t = *reinterpret_cast<const float4*>(row + q * 128 + 4 * lane);
+      dst[4 * q] = t.x, dst[4 * q + 1] = t.y, dst[4 * q + 2] = t.z, dst[4 * q + 3] = t.w;
+    }
+  } else {
+    static_assert(DPL == 2, "load_lane width");
+    const float2 t = *reinterpret_cast<const float2*>(row + 2 * lane);
+    dst[0] = t.x, dst[1] = t.y;
+  }
+}
+
+// Head held in slot 0 after warp_reduce_perm by lane `lane`: its top log2(HPW)
+// lane bits, bit-reversed.
+template <int LOG>
+__device__ __forceinline__ int perm_head(int lane) {
+  int m = 0;
+#pragma unroll
+  for (int r = 0; r < LOG; ++r) m |= ((lane >> (4 - r)) & 1) << (LOG - 1 - r);
+  return m;
+}
+
+// Warp sums of HPW per-lane values whose slot i holds head i ^ perm_head(lane):
+// halving rounds (each lane adds the partner's upper half into its lower half,
+// which with that slot order is always the same head), then butterflies.
+// Every lane returns the total of head perm_head(lane).
+template <int HPW>
+__device__ __forceinline__ float warp_reduce_perm(float (&x)[HPW]) {
+  int off = 16;
+#pragma unroll
+  for (int n = HPW; n > 1; n >>= 1, off >>= 1) {
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) x[k] += __shfl_xor_sync(0xffffffffu, x[k + n / 2], off);
+  }
+  float r = x[0];
+#pragma unroll
+  for (; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
+
+// --------------------------------------------------------------- decode_dp
+// tm_v: V as {D, n_kv, hist, seqs}, boxes {D, 1, CH, 1}.
+// tm_p, tm_s: probs / d_scores as {hist, n_heads, seqs}, boxes {CH, G, 1}.
+template <int D, int G>
+__global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
+    decode_dp_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_p,
+                     const __grid_constant__ CUtensorMap tm_s, const DecArgs a) {
+  using C = DecCfg<D, G>;
+  constexpr int CH = C::CH, NS = C::NS1, DPL = C::DPL, HPW = C::HPW, KG = C::KG, P1W = C::P1W;
+  extern __shared__ uint8_t smem_raw[];
+  // [NS][V rows [CH][D] | probs [G][CH] | probs * dp [G][CH]], 128-byte aligned
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ __align__(8) uint64_t full[NS], empty[NS];
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j_begin = split * a.keys_per_split;
-  const int j_end = min(a.hist, j_begin + a.keys_per_split);
-  const int nchunks = j_end > j_begin ? (j_end - j_begin + kDecChunk - 1) / kDecChunk : 0;
+  const long long f0 = dec_begin(blockIdx.x, a.n_chunks, a.grid);
+  const long long f1 = dec_begin(blockIdx.x + 1, a.n_chunks, a.grid);
+  const int nch = (int)(f1 - f0);
+  const int pair0 = (int)(f0 / a.cpp), lc0 = (int)(f0 % a.cpp);
 
+  if (blockIdx.x == 0)  // decode_dq's per-pair completion counters
+    for (int i = threadIdx.x; i < a.n_pairs; i += blockDim.x) a.count[i] = 0u;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], P1W);
+    }
     fence_barrier_init();
   }
   __syncthreads();
 
-  int issued = 0;            // chunks requested so far (tracked by warp 0)
-  auto issue = [&](int c) {  // warp 0: bring chunk c into stage c % kDecStages
-    const int s = c % kDecStages;
-    issued = c + 1;
-    const int j0 = j_begin + c * kDecChunk;
-    const int rows = min(kDecChunk, j_end - j0);
-    float* ks = stage_base + (size_t)s * (STAGE_BYTES / 4);
-    float* vs = ks + kDecChunk * D;
-    if (lane == 0) mbar_expect_tx(&full[s], 2u * rows * ROW_BYTES);
-    __syncwarp();
-    if (a.n_kv == 1) {
-      // the chunk's rows are contiguous: one copy per tensor
-      if (lane == 0) {
-        const size_t row = (size_t)seq * a.hist + j0;
-        bulk_load(ks, a.k + row * D, rows * ROW_BYTES, &full[s]);
-        bulk_load(vs, a.v + row * D, rows * ROW_BYTES, &full[s]);
-      }
-    } else if (lane < rows) {
-      const size_t row = ((size_t)seq * a.hist + j0 + lane) * a.n_kv + kv;
-      bulk_load(ks + lane * D, a.k + row * D, ROW_BYTES, &full[s]);
-      bulk_load(vs + lane * D, a.v + row * D, ROW_BYTES, &full[s]);
-    }
-  };
   if (warp == 0) {
-    for (int c = 0; c < kDecStages - 1 && c < nchunks; ++c) issue(c);
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      // write the probs*dp staging array of chunk c (pair pp, chunk lc) back to d_scores
+      auto park = [&](int c, int pp, int lc) {
+        tma_store_3d(&tm_s, smem + (c % NS) * C::STAGE + C::ROWS_BYTES + C::SIDE * 4, lc * CH,
+                     (pp % a.n_kv) * G, pp / a.n_kv);  // keys >= hist are clipped
+        bulk_commit();
+      };
+      bool ok = true;
+      int issued = 0;
+      int pair = pair0, lc = lc0;     // chunk c
+      int ppair = pair0, plc = lc0;   // chunk c - NS (next to write back)
+      for (int c = 0; c < nch; ++c) {
+        const int s = c % NS;
+        if (c >= NS) {
+          if (!mbar_wait(&empty[s], ((c / NS) - 1) & 1, a.err)) {
+            ok = false;
+            break;
+          }
+          if (a.side_tma) {
+            park(c - NS, ppair, plc);
+            bulk_wait_read();  // the staging array is rewritten after this chunk lands
+          }
+          if (++plc == a.cpp) plc = 0, ++ppair;
+        }
+        const int seq = pair / a.n_kv, kv = pair % a.n_kv, j0 = lc * CH;
+        uint8_t* st = smem + s * C::STAGE;
+        mbar_expect_tx(&full[s], C::ROWS_BYTES + (a.side_tma ? C::SIDE * 4u : 0u));
+        tma_load_4d(st, &tm_v, &full[s], 0, kv, j0, seq);
+        if (a.side_tma) tma_load_3d(st + C::ROWS_BYTES, &tm_p, &full[s], j0, kv * G, seq);
+        issued = c + 1;
+        if (++lc == a.cpp) lc = 0, ++pair;
+      }
+      // the last chunks: wait for their consumers, write their staging arrays back
+      for (int c = issued > NS ? issued - NS : 0; ok && c < issued; ++c) {
+        if (!mbar_wait(&empty[c % NS], (c / NS) & 1, a.err)) {
+          ok = false;
+          break;
+        }
+        if (a.side_tma) park(c, ppair, plc);
+        if (++plc == a.cpp) plc = 0, ++ppair;
+      }
+      if (!ok) {  // copies still in flight land before the CTA exits
+        for (int c = issued > NS ? issued - NS : 0; c < issued; ++c) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&full[c % NS], (c / NS) & 1) &&
+                 clock64() - t0 < kWaitLimitCycles / 4) {
+          }
+        }
+      }
+      bulk_wait_all();
+    }
+    __syncwarp();
+    return;
   }
 
-  // d_out of the G heads, lane-split over d (phase 1 operand, kept in registers)
-  float dout[G][DPL];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float* src = a.d_out + ((size_t)seq * a.n_heads + kv * G + g) * D + lane * DPL;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) dout[g][k] = src[k];
-  }
-  float sumpd_part = 0.f;  // valid in the lanes that own a head after the reduction
-  float accA[G], accB[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) accA[g] = accB[g] = 0.f;
-  uint64_t accA2[G / 2 > 0 ? G / 2 : 1], accB2[G / 2 > 0 ? G / 2 : 1];
-#pragma unroll
-  for (int i = 0; i < (G / 2 > 0 ? G / 2 : 1); ++i) accA2[i] = accB2[i] = 0;
-  const int d2 = threadIdx.x % D, kg = threadIdx.x / D;
+  // -------------------------------------------------------------- compute
+  // Warp (kgp, hg) takes keys kgp, kgp + KG, .. of every chunk for the HPW
+  // heads of head group hg.  Lane-split over d (DPL per lane), d_out in
+  // registers with slot i holding head i ^ perm_head(lane), so that
+  // warp_reduce_perm needs no selects; lane `lane` ends with head g_own.
+  const int pw = warp - 1, kgp = pw % KG, hg = pw / KG;
+  const int g_own = perm_head<C::LOG_HPW>(lane);
+  const bool owner = (lane & ((32 >> C::LOG_HPW) - 1)) == 0;  // one lane per head writes
+  float* slots = a.part1 + (size_t)blockIdx.x * a.max_seg * C::SLOT1;
+  float dout[HPW][DPL];
+  float sumpd = 0.f;
+  int cur_pair = -1, seg = -1;
+  int pair = pair0, lc = lc0;
   bool ok = true;
-  // probabilities of a chunk, G x kDecChunk values, staged one chunk ahead so
-  // phase 1 never waits on a global load
-  auto load_probs = [&](int c) {
-    if (threadIdx.x < G * kDecChunk && c < nchunks) {
-      const int g = threadIdx.x / kDecChunk, jj = threadIdx.x % kDecChunk;
-      const int j = j_begin + c * kDecChunk + jj;
-      pr_s[c & 1][jj][g] =
-          j < j_end ? a.probs[((size_t)seq * a.n_heads + kv * G + g) * a.hist + j] : 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+    const int j0 = lc * CH, rows = min(CH, a.hist - j0);
+    const int h_own = kv * G + hg * HPW + g_own;  // query head of this lane's sums
+    if (pair != cur_pair) {
+      if (seg >= 0 && owner) slots[(size_t)seg * C::SLOT1 + kgp * G + hg * HPW + g_own] = sumpd;
+      sumpd = 0.f;
+      cur_pair = pair;
+      seg = pair - pair0;
+#pragma unroll
+      for (int i = 0; i < HPW; ++i)
+        load_lane<DPL>(dout[i],
+                       a.d_out + ((size_t)seq * a.n_heads + kv * G + hg * HPW + (i ^ g_own)) * D, lane);
     }
-  };
-  load_probs(0);
+    const int s = c % NS;
+    ok = mbar_wait(&full[s], (c / NS) & 1, a.err);
+    ok = !__any_sync(0xffffffffu, !ok);
+    if (!ok) break;
+    uint8_t* st = smem + s * C::STAGE;
+    const float* vs = reinterpret_cast<const float*>(st);
+    const float* ps = reinterpret_cast<const float*>(st + C::ROWS_BYTES) + (hg * HPW + g_own) * CH;
+    float* ws = reinterpret_cast<float*>(st + C::ROWS_BYTES + C::SIDE * 4) + (hg * HPW + g_own) * CH;
+    const size_t grow = ((size_t)seq * a.n_heads + h_own) * a.hist + j0;
+    // dp of key jj for this warp's heads; the owner lanes form probs * dp
+    auto key_dp = [&](int jj) {
+      float vv[DPL];
+      load_lane<DPL>(vv, vs + jj * D, lane);
+      // packed products over consecutive d (even and odd partial sums)
+      float part[HPW];
+#pragma unroll
+      for (int i = 0; i < HPW; ++i) {
+        uint64_t acc = 0;
+#pragma unroll
+        for (int k = 0; k < DPL; k += 2)
+          acc = f2fma(pk2(dout[i][k], dout[i][k + 1]), pk2(vv[k], vv[k + 1]), acc);
+        float lo, hi;
+        up2(acc, lo, hi);
+        part[i] = lo + hi;
+      }
+      const float dp = warp_reduce_perm<HPW>(part);
+      if (owner) {
+        const float pj = a.side_tma ? ps[jj] : __ldg(a.probs + grow + jj);
+        const float w = pj * dp;
+        sumpd += w;
+        if (a.side_tma)
+          ws[jj] = w;
+        else
+          a.d_scores[grow + jj] = w;
+      }
+    };
+    if (rows == CH) {  // full chunk: no per-key branch, so the keys interleave
+#pragma unroll
+      for (int i = 0; i < CH / KG; ++i) key_dp(kgp + KG * i);
+    } else {
+      for (int i = 0; i < CH / KG; ++i)
+        if (kgp + KG * i < rows) key_dp(kgp + KG * i);  // warp-uniform
+    }
+    if (a.side_tma) fence_proxy_async_smem();  // the staging array is read by a tensor store
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++lc == a.cpp) lc = 0, ++pair;
+  }
+  if (ok && seg >= 0 && owner) slots[(size_t)seg * C::SLOT1 + kgp * G + hg * HPW + g_own] = sumpd;
+}
+
+// --------------------------------------------------------------- decode_dq
+// tm_k: K as {D, n_kv, hist, seqs}, boxes {D, 1, CH, 1}.
+template <int D, int G>
+__global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
+    decode_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_p,
+                     const __grid_constant__ CUtensorMap tm_s, const DecArgs a) {
+  using C = DecCfg<D, G>;
+  constexpr int CH = C::CH, NS = C::NS2, P2T = C::P2T, KG2 = C::KG2;
+  constexpr int P2W = P2T / 32;
+  constexpr int NACC = G == 1 ? 1 : G;  // packed accumulators
+  extern __shared__ uint8_t smem_raw[];
+  // [NS][K rows [CH][D] | parked probs * dp [G][CH] | probs [G][CH]], 128-byte aligned
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ __align__(16) float dsb[2][CH][G];  // the chunk's d_scores, key-major
+  __shared__ float sumpd_s[G];
+  __shared__ int last_s;
+  __shared__ __align__(8) uint64_t full[NS], empty[NS];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long f0 = dec_begin(blockIdx.x, a.n_chunks, a.grid);
+  const long long f1 = dec_begin(blockIdx.x + 1, a.n_chunks, a.grid);
+  const int nch = (int)(f1 - f0);
+  const int pair0 = (int)(f0 / a.cpp), lc0 = (int)(f0 % a.cpp);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], P2W);
+    }
+    fence_barrier_init();
+  }
   __syncthreads();
 
-  for (int c = 0; c < nchunks; ++c) {
-    const int s = c % kDecStages;
-    const int j0 = j_begin + c * kDecChunk;
-    const int rows = min(kDecChunk, j_end - j0);
-    // keep kDecStages - 1 chunks in flight: the stage refilled here was
-    // released by the __syncthreads that ended chunk c - 1
-    if (warp == 0 && c + kDecStages - 1 < nchunks) issue(c + kDecStages - 1);
-    load_probs(c + 1);  // visible after this chunk's closing __syncthreads
-    ok = mbar_wait(&full[s], (c / kDecStages) & 1, a.err);
-    const float* ks = stage_base + (size_t)s * (STAGE_BYTES / 4);
-    const float* vs = ks + kDecChunk * D;
-    // phase 1: dp for the G heads, one key per warp at a time (unrolled so the
-    // shuffle chains of a warp's keys interleave)
-#pragma unroll
-    for (int jj = warp; jj < kDecChunk; jj += kDecThreads / 32) {
-      float part[G];
-      if (jj < rows) {
-        float vv[DPL];
-#pragma unroll
-        for (int k = 0; k < DPL; k += 4) {
-          const float4 t = *reinterpret_cast<const float4*>(vs + jj * D + lane * DPL + k);
-          vv[k] = t.x;
-          if (k + 1 < DPL) vv[k + 1] = t.y;
-          if (k + 2 < DPL) vv[k + 2] = t.z;
-          if (k + 3 < DPL) vv[k + 3] = t.w;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      int pair = pair0, lc = lc0;  // chunk c
+      for (int c = 0; c < nch; ++c) {
+        const int s = c % NS;
+        if (c >= NS && !mbar_wait(&empty[s], ((c / NS) - 1) & 1, a.err)) break;
+        const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+        const int j0 = lc * CH;
+        if (++lc == a.cpp) lc = 0, ++pair;
+        uint8_t* st = smem + s * C::STAGE;
+        mbar_expect_tx(&full[s], C::ROWS_BYTES + (a.side_tma ? 2u * C::SIDE * 4u : 0u));
+        tma_load_4d(st, &tm_k, &full[s], 0, kv, j0, seq);
+        if (a.side_tma) {
+          tma_load_3d(st + C::ROWS_BYTES, &tm_s, &full[s], j0, kv * G, seq);
+          tma_load_3d(st + C::ROWS_BYTES + C::SIDE * 4, &tm_p, &full[s], j0, kv * G, seq);
         }
-        if constexpr (G % 2 == 0) {
-          // two heads per packed fma
-#pragma unroll
-          for (int g = 0; g < G; g += 2) {
-            uint64_t acc = 0;
-#pragma unroll
-            for (int k = 0; k < DPL; ++k)
-              acc = f2fma(pk2(dout[g][k], dout[g + 1][k]), pk2(vv[k], vv[k]), acc);
-            up2(acc, part[g], part[g + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float acc = 0.f;
-#pragma unroll
-            for (int k = 0; k < DPL; ++k) acc = fmaf(dout[g][k], vv[k], acc);
-            part[g] = acc;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = 0.f;
+        issued = c + 1;
       }
-      const float dp = warp_reduce_scatter<G>(part, lane);
-      const int g = lane >> (5 - LOG_G);
-      if ((lane & ((32 >> LOG_G) - 1)) == 0) {
-        float w1 = 0.f;
-        if (jj < rows) {
-          const size_t idx = ((size_t)seq * a.n_heads + kv * G + g) * a.hist + j0 + jj;
-          w1 = pr_s[c & 1][jj][g] * dp;
-          a.d_scores[idx] = dp;  // parked; finalize turns it into d_scores
-          sumpd_part += w1;
+      // copies still in flight land before the CTA exits
+      for (int c = issued > NS ? issued - NS : 0; c < issued; ++c) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&full[c % NS], (c / NS) & 1) && clock64() - t0 < kWaitLimitCycles / 4) {
         }
-        w1_s[jj][g] = w1;
       }
     }
-    // block-uniform exit if any thread's wait gave up (error path only)
-    if (__syncthreads_or(!ok)) {
+    __syncwarp();
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  // thread t2 owns d, d + 1 for the keys kg, kg + KG2, ... of every chunk.
+  // For even G the packed accumulators pair consecutive heads:
+  // acc[hp] = (d_q[2hp][d], d_q[2hp+1][d]), acc[G/2 + hp] the same at d + 1;
+  // for G = 1, acc[0] = (d_q[0][d], d_q[0][d+1]).
+  const int t2 = threadIdx.x - 32;
+  const int kg = t2 / (D / 2), d = 2 * (t2 % (D / 2));
+  float* slots = a.part2 + (size_t)blockIdx.x * a.max_seg * C::SLOT2;
+  uint64_t acc[NACC];
+#pragma unroll
+  for (int i = 0; i < NACC; ++i) acc[i] = 0;
+  int cur_pair = -1, seg = -1;
+  bool ok = true;
+
+  // segment `seg` (pair cur_pair) is complete in this CTA
+  auto finish = [&]() {
+    float* sl = slots + (size_t)seg * C::SLOT2 + (size_t)kg * G * D;
+    if constexpr (G == 1) {
+      float x0, x1;
+      up2(acc[0], x0, x1);
+      *reinterpret_cast<float2*>(sl + d) = make_float2(x0, x1);
+    } else {
+#pragma unroll
+      for (int hp = 0; hp < G / 2; ++hp) {
+        float a0, a1, b0, b1;
+        up2(acc[hp], a0, a1);
+        up2(acc[G / 2 + hp], b0, b1);
+        *reinterpret_cast<float2*>(sl + (2 * hp) * D + d) = make_float2(a0, b0);
+        *reinterpret_cast<float2*>(sl + (2 * hp + 1) * D + d) = make_float2(a1, b1);
+      }
+    }
+    __threadfence();
+    named_bar_sync(1, P2T);
+    const long long fa = (long long)cur_pair * a.cpp;
+    const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+    const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+    if (t2 == 0)
+      last_s = ia == ib || atomicAdd(&a.count[cur_pair], 1u) == (unsigned)(ib - ia);
+    named_bar_sync(1, P2T);
+    if (last_s) {  // every CTA of the pair has written its partial: sum in CTA order
+      __threadfence();
+      const int seq = cur_pair / a.n_kv, kv = cur_pair % a.n_kv;
+      for (int o = t2; o < G * D; o += P2T) {
+        const int g = o / D, dd = o % D;
+        float t = 0.f;
+        for (int i = ia; i <= ib; ++i) {
+          const int sg = cur_pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
+          const float* p2 = a.part2 + ((size_t)i * a.max_seg + sg) * C::SLOT2 + g * D + dd;
+          for (int q = 0; q < KG2; ++q) t += __ldcg(p2 + (size_t)q * G * D);
+        }
+        a.d_q[((size_t)seq * a.n_heads + kv * G + g) * D + dd] = t;
+      }
+    }
+  };
+
+  int pair = pair0, lc = lc0;
+  for (int c = 0; c < nch; ++c) {
+    const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+    const int j0 = lc * CH, rows = min(CH, a.hist - j0);
+    if (pair != cur_pair) {
+      if (seg >= 0) finish();
+      cur_pair = pair;
+      seg = pair - pair0;
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) acc[i] = 0;
+      if (t2 < G) {  // sum_pd of the pair from decode_dp's partials
+        const long long fa = (long long)pair * a.cpp;
+        const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+        const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+        float t = 0.f;
+        for (int i = ia; i <= ib; ++i) {
+          const int sg = pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
+          const float* p1 = a.part1 + ((size_t)i * a.max_seg + sg) * C::SLOT1;
+          for (int q = 0; q < C::KG; ++q) t += p1[q * G + t2];
+        }
+        sumpd_s[t2] = t;
+      }
+      named_bar_sync(1, P2T);
+    }
+    const int s = c % NS, b = c & 1;
+    ok = mbar_wait(&full[s], (c / NS) & 1, a.err);
+    const float* ks = reinterpret_cast<const float*>(smem + s * C::STAGE);
+    if (ok) {
+      // the chunk's final d_scores: consecutive threads take consecutive keys of a head
+      const float* wsd = ks + CH * D;
+      const float* psd = wsd + C::SIDE;
+      for (int i = t2; i < G * CH; i += P2T) {
+        const int g = i / CH, jj = i % CH;
+        if (jj < rows) {
+          const size_t gi = ((size_t)seq * a.n_heads + kv * G + g) * a.hist + j0 + jj;
+          const float w = a.side_tma ? wsd[g * CH + jj] : a.d_scores[gi];
+          const float pv = a.side_tma ? psd[g * CH + jj] : __ldg(a.probs + gi);
+          const float ds = fmaf(-pv, sumpd_s[g], w);
+          a.d_scores[gi] = ds;
+          dsb[b][jj][g] = ds;
+        }
+      }
+    }
+    if (named_bar_or(1, P2T, !ok)) {
       ok = false;
       break;
     }
-    // phase 2: A += (probs dp) k, B += probs k, thread per d; heads in pairs
-    // with packed fma, weights of a key read as vectors (keys past `rows`
-    // carry zero weights)
-    for (int jj = kg; jj < rows; jj += NKG) {
-      const float kval = ks[jj * D + d2];
-      if constexpr (G % 2 == 0) {
-        const uint64_t k2 = pk2(kval, kval);
-        const uint64_t* w2 = reinterpret_cast<const uint64_t*>(&w1_s[jj][0]);
-        const uint64_t* p2 = reinterpret_cast<const uint64_t*>(&pr_s[c & 1][jj][0]);
-#pragma unroll
-        for (int i = 0; i < G / 2; ++i) {
-          accA2[i] = f2fma(w2[i], k2, accA2[i]);
-          accB2[i] = f2fma(p2[i], k2, accB2[i]);
-        }
+    auto key_dq = [&](int jj) {
+      const float2 kk = *reinterpret_cast<const float2*>(ks + jj * D + d);
+      if constexpr (G == 1) {
+        const float dv = dsb[b][jj][0];
+        acc[0] = f2fma(pk2(dv, dv), pk2(kk.x, kk.y), acc[0]);
       } else {
+        const uint64_t k0 = pk2(kk.x, kk.x), k1 = pk2(kk.y, kk.y);
+        if constexpr (G == 2) {
+          const uint64_t t = *reinterpret_cast<const uint64_t*>(&dsb[b][jj][0]);
+          acc[0] = f2fma(t, k0, acc[0]);
+          acc[1] = f2fma(t, k1, acc[1]);
+        } else {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          accA[g] = fmaf(w1_s[jj][g], kval, accA[g]);
-          accB[g] = fmaf(pr_s[c & 1][jj][g], kval, accB[g]);
+          for (int hp = 0; hp < G / 2; hp += 2) {
+            const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(&dsb[b][jj][2 * hp]);
+            acc[hp] = f2fma(t.x, k0, acc[hp]);
+            acc[G / 2 + hp] = f2fma(t.x, k1, acc[G / 2 + hp]);
+            acc[hp + 1] = f2fma(t.y, k0, acc[hp + 1]);
+            acc[G / 2 + hp + 1] = f2fma(t.y, k1, acc[G / 2 + hp + 1]);
+          }
         }
       }
-    }
-    __syncthreads();  // stage s and w1_s / pr_s are free again
-  }
-
-  if constexpr (G % 2 == 0) {
+    };
+    if (rows == CH) {
 #pragma unroll
-    for (int i = 0; i < G / 2; ++i) {
-      up2(accA2[i], accA[2 * i], accA[2 * i + 1]);
-      up2(accB2[i], accB[2 * i], accB[2 * i + 1]);
+      for (int i = 0; i < CH / KG2; ++i) key_dq(kg + KG2 * i);
+    } else {
+      for (int jj = kg; jj < rows; jj += KG2) key_dq(jj);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++lc == a.cpp) lc = 0, ++pair;
   }
-  // per-warp sum_pd partials -> smem
-  {
-    const int g = lane >> (5 - LOG_G);
-    if ((lane & ((32 >> LOG_G) - 1)) == 0) sumpd_s[warp][g] = sumpd_part;
-  }
-  if (NKG > 1) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      red_s[kg][g][d2] = accA[g];
-      red_s[kg][G + g][d2] = accB[g];
-    }
-  }
-  __syncthreads();
-  float* out = a.partials + ((size_t)pair * a.n_split + split) * G * (1 + 2 * D);
-  if (threadIdx.x < G) {
-    float t = 0.f;
-    for (int w = 0; w < kDecThreads / 32; ++w) t += sumpd_s[w][threadIdx.x];
-    out[threadIdx.x * (1 + 2 * D)] = ok ? t : 0.f;
-  }
-  if (kg == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float sa = accA[g], sb = accB[g];
-      for (int q = 1; q < NKG; ++q) {
-        sa += red_s[q][g][d2];
-        sb += red_s[q][G + g][d2];
-      }
-      out[g * (1 + 2 * D) + 1 + d2] = sa;
-      out[g * (1 + 2 * D) + 1 + D + d2] = sb;
-    }
-  }
-  // copies still in flight (only when a wait gave up) must land before exit
-  if (!ok && threadIdx.x == 0) {
-    for (int c = issued > kDecStages ? issued - kDecStages : 0; c < issued; ++c) {
-      long long t0 = clock64();
-      while (!mbar_try_wait(&full[c % kDecStages], (c / kDecStages) & 1) &&
-             clock64() - t0 < kWaitLimitCycles / 4) {
-      }
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256) decode_finalize_kernel(const DecArgs a, int G) {
-  const int h = blockIdx.x, seq = blockIdx.y;
-  const int kv = h / G, g = h % G;
-  const int pair = seq * a.n_kv + kv;
-  const int D = a.D;
-  const float* base = a.partials + (size_t)pair * a.n_split * G * (1 + 2 * D);
-  __shared__ float sumpd_sh;
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int s = 0; s < a.n_split; ++s) t += base[((size_t)s * G + g) * (1 + 2 * D)];
-    sumpd_sh = t;
-  }
-  __syncthreads();
-  const float sumpd = sumpd_sh;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float A = 0.f, Bs = 0.f;
-    for (int s = 0; s < a.n_split; ++s) {
-      const float* pp = base + ((size_t)s * G + g) * (1 + 2 * D);
-      A += pp[1 + d];
-      Bs += pp[1 + D + d];
-    }
-    a.d_q[((size_t)seq * a.n_heads + h) * D + d] = A - sumpd * Bs;
-  }
-  const size_t row = ((size_t)seq * a.n_heads + h) * a.hist;
-  for (int j = threadIdx.x; j < a.hist; j += blockDim.x) {
-    const float dp = a.d_scores[row + j];
-    a.d_scores[row + j] = a.probs[row + j] * (dp - sumpd);
-  }
+  if (ok && seg >= 0) finish();
 }
 
 template <int D, int G>
-cudaError_t main_impl(const DecArgs& a, dim3 grid, cudaStream_t stream) {
-  const int smem = kDecStages * 2 * kDecChunk * D * 4;
-  auto kern = decode_main_kernel<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t decode_impl(const DecArgs& a, cudaStream_t stream) {
+  using C = DecCfg<D, G>;
+  const long long seqs = a.n_pairs / a.n_kv;
+  CUtensorMap tm_v, tm_k, tm_p, tm_s;
+  memset(&tm_p, 0, sizeof(tm_p));
+  memset(&tm_s, 0, sizeof(tm_s));
+  {
+    const long long dims[4] = {D, a.n_kv, a.hist, seqs};
+    const int box[4] = {D, 1, C::CH, 1};
+    if (make_f32_map(&tm_v, a.v, 4, dims, box, false) != CUDA_SUCCESS ||
+        make_f32_map(&tm_k, a.k, 4, dims, box, false) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (a.side_tma) {
+    const long long dims[3] = {a.hist, a.n_heads, seqs};
+    const int box[3] = {C::CH, G, 1};
+    if (make_f32_map(&tm_p, a.probs, 3, dims, box, false) != CUDA_SUCCESS ||
+        make_f32_map(&tm_s, a.d_scores, 3, dims, box, false) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  auto k1 = decode_dp_kernel<D, G>;
+  auto k2 = decode_dq_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM2);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecThreads, smem, stream>>>(a);
+  k1<<<a.grid, 32 * (1 + C::P1W), C::SMEM1, stream>>>(tm_v, tm_p, tm_s, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k2<<<a.grid, 32 + C::P2T, C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
   return cudaGetLastError();
 }
 
+template <int D, int G>
+void decode_slots(int& s1, int& s2) {
+  s1 = DecCfg<D, G>::SLOT1;
+  s2 = DecCfg<D, G>::SLOT2;
+}
+
+// Slot sizes of the two kernels for a supported (D, G); false otherwise.
 template <int D>
-cudaError_t main_by_group(const DecArgs& a, int G, dim3 grid, cudaStream_t stream) {
+bool dec_slots_by_group(int G, int& s1, int& s2) {
   switch (G) {
-    case 1: return main_impl<D, 1>(a, grid, stream);
-    case 2: return main_impl<D, 2>(a, grid, stream);
-    case 4: return main_impl<D, 4>(a, grid, stream);
-    case 8: return main_impl<D, 8>(a, grid, stream);
-    case 16: return main_impl<D, 16>(a, grid, stream);
+    case 1: decode_slots<D, 1>(s1, s2); return true;
+    case 2: decode_slots<D, 2>(s1, s2); return true;
+    case 4: decode_slots<D, 4>(s1, s2); return true;
+    case 8: decode_slots<D, 8>(s1, s2); return true;
+    case 16: decode_slots<D, 16>(s1, s2); return true;
+    default: return false;
+  }
+}
+bool dec_slots(int D, int G, int& s1, int& s2) {
+  switch (D) {
+    case 64: return dec_slots_by_group<64>(G, s1, s2);
+    case 128: return dec_slots_by_group<128>(G, s1, s2);
+    case 256: return dec_slots_by_group<256>(G, s1, s2);
+    default: return false;
+  }
+}
+
+template <int D>
+cudaError_t decode_by_group(const DecArgs& a, int G, cudaStream_t stream) {
+  switch (G) {
+    case 1: return decode_impl<D, 1>(a, stream);
+    case 2: return decode_impl<D, 2>(a, stream);
+    case 4: return decode_impl<D, 4>(a, stream);
+    case 8: return decode_impl<D, 8>(a, stream);
+    case 16: return decode_impl<D, 16>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-}  // namespace
-
-int decode_num_splits(const attn_bwd_decode_params& p) {
-  const long long pairs = (long long)p.num_seqs * p.n_kv_heads;
-  long long s = kDecSlots / (pairs > 0 ? pairs : 1);
-  const long long max_s = (p.history_len + kDecChunk - 1) / kDecChunk;
-  if (s > max_s) s = max_s;
-  if (s < 1) s = 1;
-  return (int)s;
+long long dec_chunks(const attn_bwd_decode_params& p) {
+  const long long cpp = (p.history_len + kDecChunk - 1) / kDecChunk;
+  return (long long)p.num_seqs * p.n_kv_heads * cpp;
 }
 
+// Partial slots one CTA needs: the most (sequence, KV head) pairs a range of
+// ceil(n / grid) chunks can touch.
+int dec_max_seg(const attn_bwd_decode_params& p, int grid) {
+  const long long cpp = (p.history_len + kDecChunk - 1) / kDecChunk;
+  const long long n = dec_chunks(p);
+  const long long per = (n + grid - 1) / grid;
+  return (int)((per + cpp - 1) / cpp + 1);
+}
+
+}  // namespace
+
+// Number of CTAs of either decode kernel: one per SM of the current device
+// (152 when no device can be queried), at most one per chunk.
+int decode_num_splits(const attn_bwd_decode_params& p) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();  // clear the error of a host without a device
+    sms = kDecSmsFallback;
+  }
+  const long long n = dec_chunks(p);
+  return (int)(n < sms ? n : sms);
+}
+
+// Workspace floats: both kernels' partial slots, then one counter per pair.
 size_t decode_partials_floats(const attn_bwd_decode_params& p, int n_split) {
-  const int G = p.n_heads / p.n_kv_heads;
-  return (size_t)p.num_seqs * p.n_kv_heads * n_split * G * (1 + 2 * (size_t)p.head_dim);
+  int s1 = 0, s2 = 0;
+  if (!dec_slots(p.head_dim, p.n_heads / p.n_kv_heads, s1, s2)) return 0;
+  const size_t per_cta = (size_t)dec_max_seg(p, n_split) * (s1 + s2);
+  return (size_t)n_split * per_cta + (size_t)p.num_seqs * p.n_kv_heads;
 }
 
 cudaError_t launch_decode(const attn_bwd_decode_params& p, const float* k_hist,
                           const float* v_hist, const float* probs, const float* d_out,
                           float* d_scores, float* d_q, float* partials, int n_split,
                           cudaStream_t stream) {
+  const int G = p.n_heads / p.n_kv_heads;
+  int s1 = 0, s2 = 0;
+  if (!dec_slots(p.head_dim, G, s1, s2)) return cudaErrorInvalidValue;
   DecArgs a;
   a.k = k_hist;
   a.v = v_hist;
@@ -396,28 +728,30 @@ cudaError_t launch_decode(const attn_bwd_decode_params& p, const float* k_hist,
   a.d_out = d_out;
   a.d_scores = d_scores;
   a.d_q = d_q;
-  a.partials = partials;
   a.n_heads = p.n_heads;
   a.n_kv = p.n_kv_heads;
   a.D = p.head_dim;
   a.hist = p.history_len;
-  a.n_split = n_split;
-  const int per = (p.history_len + n_split - 1) / n_split;
-  a.keys_per_split = (per + kDecChunk - 1) / kDecChunk * kDecChunk;
+  a.cpp = (p.history_len + kDecChunk - 1) / kDecChunk;
+  a.n_pairs = p.num_seqs * p.n_kv_heads;
+  a.n_chunks = dec_chunks(p);
+  a.grid = n_split;
+  a.max_seg = dec_max_seg(p, n_split);
+  a.part1 = partials;
+  a.part2 = partials + (size_t)n_split * a.max_seg * s1;
+  a.count = reinterpret_cast<unsigned int*>(a.part2 + (size_t)n_split * a.max_seg * s2);
+  // the [.., hist] tensor maps need a 16-byte row stride (every pointer is
+  // 16-byte aligned, checked by the API)
+  a.side_tma = p.history_len % 4 == 0;
   a.err = device_error_word();
   if (!a.err) return cudaErrorUnknown;
-  const int G = p.n_heads / p.n_kv_heads;
-  dim3 grid(n_split, p.num_seqs * p.n_kv_heads);
-  cudaError_t e;
+  if (a.grid < 1 || a.grid > a.n_chunks) return cudaErrorInvalidValue;
   switch (p.head_dim) {
-    case 64: e = main_by_group<64>(a, G, grid, stream); break;
-    case 128: e = main_by_group<128>(a, G, grid, stream); break;
-    case 256: e = main_by_group<256>(a, G, grid, stream); break;
+    case 64: return decode_by_group<64>(a, G, stream);
+    case 128: return decode_by_group<128>(a, G, stream);
+    case 256: return decode_by_group<256>(a, G, stream);
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  decode_finalize_kernel<<<dim3(p.n_heads, p.num_seqs), 256, 0, stream>>>(a, G);
-  return cudaGetLastError();
 }
 
 }  // namespace attnbwd

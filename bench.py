@@ -520,8 +520,8 @@ def run_decode(args):
             "roofline": {"bound": "hbm", "achieved": nbytes / (mean_ms * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s",
                          "frac": nbytes / (mean_ms * 1e-3) / 1e9 / peak,
-                         "traffic": read_traffic("main", prefix="decode_"),
-                         "kernel": "decode_main_kernel + decode_finalize_kernel",
+                         "traffic": read_traffic("passes", prefix="decode_"),
+                         "kernel": "decode_dp_kernel + decode_dq_kernel",
                          "peak_source": f"{src} hbm_gbs"},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clocks,
         }
