@@ -174,15 +174,19 @@ struct DecCfg {
   static constexpr int SMEM1 = NS1 * STAGE + 128;             // + alignment slack
   static constexpr int SLOT1 = KG * G;                        // sum_pd[KG][G]
   // decode_dq: stage = [K rows [CH][D] | parked probs*dp | probs]
-  static constexpr int P2T = 256;                         // compute threads
-  static constexpr int KG2 = P2T * 2 / D;                 // key groups (two d per thread)
-  static constexpr int NS2 = dec_clamp((kDecSmemMax - 2048 - (2 * CH * G + G) * 4) / STAGE, 2, 12);
+  static constexpr int P2W = 8;                           // accumulating warps
+  static constexpr int P2T = 32 * P2W;
+  static constexpr int DPT = 4;                           // d per accumulating thread
+  static constexpr int KG2 = P2T * DPT / D;               // key groups
+  static constexpr int NB = 4;                            // d_scores buffers
+  static constexpr int DSB_BYTES = NB * CH * G * 4;
+  static constexpr int NS2 = dec_clamp((kDecSmemMax - 2048 - DSB_BYTES) / STAGE, 2, 12);
   static constexpr int SMEM2 = NS2 * STAGE + 128;
   static constexpr int SLOT2 = KG2 * G * D;               // d_q[KG2][G][D]
   static_assert(HPW * DPL <= 64 && G % HPW == 0 && KG >= 1 && CH % KG == 0 && D % 64 == 0 &&
                     D <= 256, "decode_dp split");
   static_assert(KG2 >= 1 && CH % KG2 == 0, "decode_dq split");
-  static_assert(SMEM1 + 1024 <= kDecSmemMax && SMEM2 + (2 * CH * G + G) * 4 + 1024 <= kDecSmemMax,
+  static_assert(SMEM1 + 1024 <= kDecSmemMax && SMEM2 + DSB_BYTES + 1024 <= kDecSmemMax,
                 "decode shared memory");
 };
 
@@ -358,8 +362,9 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
     const float* ps = reinterpret_cast<const float*>(st + C::ROWS_BYTES) + (hg * HPW + g_own) * CH;
     float* ws = reinterpret_cast<float*>(st + C::ROWS_BYTES + C::SIDE * 4) + (hg * HPW + g_own) * CH;
     const size_t grow = ((size_t)seq * a.n_heads + h_own) * a.hist + j0;
-    // dp of key jj for this warp's heads; the owner lanes form probs * dp
-    auto key_dp = [&](int jj) {
+    // dp of key jj for this warp's heads (every lane; no branch, so that the
+    // keys of a chunk interleave)
+    auto key_dot = [&](int jj) {
       float vv[DPL];
       load_lane<DPL>(vv, vs + jj * D, lane);
       // packed products over consecutive d (even and odd partial sums)
@@ -374,23 +379,33 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
         up2(acc, lo, hi);
         part[i] = lo + hi;
       }
-      const float dp = warp_reduce_perm<HPW>(part);
-      if (owner) {
-        const float pj = a.side_tma ? ps[jj] : __ldg(a.probs + grow + jj);
-        const float w = pj * dp;
-        sumpd += w;
-        if (a.side_tma)
-          ws[jj] = w;
-        else
-          a.d_scores[grow + jj] = w;
-      }
+      return warp_reduce_perm<HPW>(part);
     };
-    if (rows == CH) {  // full chunk: no per-key branch, so the keys interleave
+    // the owner lanes form probs * dp
+    auto own = [&](int jj, float dp) {
+      const float pj = a.side_tma ? ps[jj] : __ldg(a.probs + grow + jj);
+      const float w = pj * dp;
+      sumpd += w;
+      if (a.side_tma)
+        ws[jj] = w;
+      else
+        a.d_scores[grow + jj] = w;
+    };
+    if (rows == CH) {  // full chunk
+      float dps[CH / KG];
 #pragma unroll
-      for (int i = 0; i < CH / KG; ++i) key_dp(kgp + KG * i);
+      for (int i = 0; i < CH / KG; ++i) dps[i] = key_dot(kgp + KG * i);
+      if (owner) {
+#pragma unroll
+        for (int i = 0; i < CH / KG; ++i) own(kgp + KG * i, dps[i]);
+      }
     } else {
-      for (int i = 0; i < CH / KG; ++i)
-        if (kgp + KG * i < rows) key_dp(kgp + KG * i);  // warp-uniform
+      for (int i = 0; i < CH / KG; ++i) {
+        if (kgp + KG * i < rows) {  // warp-uniform
+          const float dp = key_dot(kgp + KG * i);
+          if (owner) own(kgp + KG * i, dp);
+        }
+      }
     }
     if (a.side_tma) fence_proxy_async_smem();  // the staging array is read by a tensor store
     __syncwarp();
@@ -402,22 +417,24 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
 
 // --------------------------------------------------------------- decode_dq
 // tm_k: K as {D, n_kv, hist, seqs}, boxes {D, 1, CH, 1}.
+// Warps: 0 producer; 1 .. P2W accumulate d_q (P2T threads, DPT = 4 d each,
+// KG2 key groups); P2W + 1 forms each chunk's d_scores into a ring of NB
+// shared buffers, one chunk ahead of the accumulating warps.
 template <int D, int G>
-__global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
+__global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
     decode_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_p,
                      const __grid_constant__ CUtensorMap tm_s, const DecArgs a) {
   using C = DecCfg<D, G>;
-  constexpr int CH = C::CH, NS = C::NS2, P2T = C::P2T, KG2 = C::KG2;
-  constexpr int P2W = P2T / 32;
-  constexpr int NACC = G == 1 ? 1 : G;  // packed accumulators
+  constexpr int CH = C::CH, NS = C::NS2, NB = C::NB, P2T = C::P2T, P2W = C::P2W, KG2 = C::KG2;
+  constexpr int DPT = C::DPT;
+  constexpr int NACC = G == 1 ? DPT / 2 : DPT * (G / 2);  // packed accumulators
   extern __shared__ uint8_t smem_raw[];
   // [NS][K rows [CH][D] | parked probs * dp [G][CH] | probs [G][CH]], 128-byte aligned
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ __align__(16) float dsb[2][CH][G];  // the chunk's d_scores, key-major
-  __shared__ float sumpd_s[G];
+  __shared__ __align__(16) float dsb[NB][CH][G];  // chunks' d_scores, key-major
   __shared__ int last_s;
-  __shared__ __align__(8) uint64_t full[NS], empty[NS];
+  __shared__ __align__(8) uint64_t full[NS], empty[NS], ds_full[NB], ds_empty[NB];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long f0 = dec_begin(blockIdx.x, a.n_chunks, a.grid);
@@ -428,7 +445,11 @@ __global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], P2W);
+      mbar_init(&empty[s], P2W + 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&ds_full[b], 32);
+      mbar_init(&ds_empty[b], P2W);
     }
     fence_barrier_init();
   }
@@ -465,13 +486,69 @@ __global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
     return;
   }
 
-  // -------------------------------------------------------------- compute
-  // thread t2 owns d, d + 1 for the keys kg, kg + KG2, ... of every chunk.
+  if (warp == 1 + P2W) {
+    // ------------------------------------------------------- d_scores warp
+    // lane j = key j of the chunk: d_scores = probs*dp - probs * sum_pd for
+    // every head, stored to global memory and to dsb
+    float sp[G];  // sum_pd of the current pair, every head
+    int cur = -1;
+    int pair = pair0, lc = lc0;
+    for (int c = 0; c < nch; ++c) {
+      const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+      const int j0 = lc * CH, rows = min(CH, a.hist - j0);
+      if (pair != cur) {  // sum_pd of the pair from decode_dp's partials
+        cur = pair;
+        float v = 0.f;
+        if (lane < G) {
+          const long long fa = (long long)pair * a.cpp;
+          const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+          const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+          for (int i = ia; i <= ib; ++i) {
+            const int sg = pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
+            const float* p1 = a.part1 + ((size_t)i * a.max_seg + sg) * C::SLOT1;
+            for (int q = 0; q < C::KG; ++q) v += p1[q * G + lane];
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) sp[g] = __shfl_sync(0xffffffffu, v, g);
+      }
+      const int s = c % NS, b = c % NB;
+      bool ok = mbar_wait(&full[s], (c / NS) & 1, a.err) &&
+                (c < NB || mbar_wait(&ds_empty[b], ((c / NB) - 1) & 1, a.err));
+      if (__any_sync(0xffffffffu, !ok)) break;
+      const float* wsd = reinterpret_cast<const float*>(smem + s * C::STAGE + C::ROWS_BYTES);
+      const float* psd = wsd + C::SIDE;
+      const bool in = lane < rows;
+      const size_t gi0 = ((size_t)seq * a.n_heads + kv * G) * a.hist + j0 + lane;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float w, pv;
+        if (a.side_tma) {
+          w = wsd[g * CH + lane];
+          pv = psd[g * CH + lane];
+        } else {
+          w = in ? a.d_scores[gi0 + (size_t)g * a.hist] : 0.f;
+          pv = in ? __ldg(a.probs + gi0 + (size_t)g * a.hist) : 0.f;
+        }
+        const float ds = fmaf(-pv, sp[g], w);
+        if (in) a.d_scores[gi0 + (size_t)g * a.hist] = ds;
+        dsb[b][lane][g] = ds;
+      }
+      mbar_arrive(&ds_full[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++lc == a.cpp) lc = 0, ++pair;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------- accumulators
+  // thread t2 owns d .. d + 3 for the keys kg, kg + KG2, ... of every chunk.
   // For even G the packed accumulators pair consecutive heads:
-  // acc[hp] = (d_q[2hp][d], d_q[2hp+1][d]), acc[G/2 + hp] the same at d + 1;
-  // for G = 1, acc[0] = (d_q[0][d], d_q[0][d+1]).
+  // acc[i (G/2) + hp] = (d_q[2hp][d + i], d_q[2hp+1][d + i]); for G = 1,
+  // acc[i] = (d_q[0][d + 2i], d_q[0][d + 2i + 1]).
   const int t2 = threadIdx.x - 32;
-  const int kg = t2 / (D / 2), d = 2 * (t2 % (D / 2));
+  const int kg = t2 / (D / DPT), d = DPT * (t2 % (D / DPT));
   float* slots = a.part2 + (size_t)blockIdx.x * a.max_seg * C::SLOT2;
   uint64_t acc[NACC];
 #pragma unroll
@@ -481,21 +558,20 @@ __global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
 
   // segment `seg` (pair cur_pair) is complete in this CTA
   auto finish = [&]() {
-    float* sl = slots + (size_t)seg * C::SLOT2 + (size_t)kg * G * D;
+    float x[G][DPT];
     if constexpr (G == 1) {
-      float x0, x1;
-      up2(acc[0], x0, x1);
-      *reinterpret_cast<float2*>(sl + d) = make_float2(x0, x1);
+#pragma unroll
+      for (int i = 0; i < DPT / 2; ++i) up2(acc[i], x[0][2 * i], x[0][2 * i + 1]);
     } else {
 #pragma unroll
-      for (int hp = 0; hp < G / 2; ++hp) {
-        float a0, a1, b0, b1;
-        up2(acc[hp], a0, a1);
-        up2(acc[G / 2 + hp], b0, b1);
-        *reinterpret_cast<float2*>(sl + (2 * hp) * D + d) = make_float2(a0, b0);
-        *reinterpret_cast<float2*>(sl + (2 * hp + 1) * D + d) = make_float2(a1, b1);
-      }
+      for (int i = 0; i < DPT; ++i)
+#pragma unroll
+        for (int hp = 0; hp < G / 2; ++hp) up2(acc[i * (G / 2) + hp], x[2 * hp][i], x[2 * hp + 1][i]);
     }
+    float* sl = slots + (size_t)seg * C::SLOT2 + (size_t)kg * G * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      *reinterpret_cast<float4*>(sl + g * D + d) = make_float4(x[g][0], x[g][1], x[g][2], x[g][3]);
     __threadfence();
     named_bar_sync(1, P2T);
     const long long fa = (long long)cur_pair * a.cpp;
@@ -522,72 +598,45 @@ __global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
 
   int pair = pair0, lc = lc0;
   for (int c = 0; c < nch; ++c) {
-    const int seq = pair / a.n_kv, kv = pair % a.n_kv;
-    const int j0 = lc * CH, rows = min(CH, a.hist - j0);
+    const int rows = min(CH, a.hist - lc * CH);
     if (pair != cur_pair) {
       if (seg >= 0) finish();
       cur_pair = pair;
       seg = pair - pair0;
 #pragma unroll
       for (int i = 0; i < NACC; ++i) acc[i] = 0;
-      if (t2 < G) {  // sum_pd of the pair from decode_dp's partials
-        const long long fa = (long long)pair * a.cpp;
-        const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
-        const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
-        float t = 0.f;
-        for (int i = ia; i <= ib; ++i) {
-          const int sg = pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
-          const float* p1 = a.part1 + ((size_t)i * a.max_seg + sg) * C::SLOT1;
-          for (int q = 0; q < C::KG; ++q) t += p1[q * G + t2];
-        }
-        sumpd_s[t2] = t;
-      }
-      named_bar_sync(1, P2T);
     }
-    const int s = c % NS, b = c & 1;
-    ok = mbar_wait(&full[s], (c / NS) & 1, a.err);
-    const float* ks = reinterpret_cast<const float*>(smem + s * C::STAGE);
-    if (ok) {
-      // the chunk's final d_scores: consecutive threads take consecutive keys of a head
-      const float* wsd = ks + CH * D;
-      const float* psd = wsd + C::SIDE;
-      for (int i = t2; i < G * CH; i += P2T) {
-        const int g = i / CH, jj = i % CH;
-        if (jj < rows) {
-          const size_t gi = ((size_t)seq * a.n_heads + kv * G + g) * a.hist + j0 + jj;
-          const float w = a.side_tma ? wsd[g * CH + jj] : a.d_scores[gi];
-          const float pv = a.side_tma ? psd[g * CH + jj] : __ldg(a.probs + gi);
-          const float ds = fmaf(-pv, sumpd_s[g], w);
-          a.d_scores[gi] = ds;
-          dsb[b][jj][g] = ds;
-        }
-      }
-    }
-    if (named_bar_or(1, P2T, !ok)) {
+    const int s = c % NS, b = c % NB;
+    ok = mbar_wait(&full[s], (c / NS) & 1, a.err) && mbar_wait(&ds_full[b], (c / NB) & 1, a.err);
+    if (named_bar_or(1, P2T, !ok)) {  // every accumulating thread leaves together
       ok = false;
       break;
     }
+    const float* ks = reinterpret_cast<const float*>(smem + s * C::STAGE);
     auto key_dq = [&](int jj) {
-      const float2 kk = *reinterpret_cast<const float2*>(ks + jj * D + d);
+      const float4 kk = *reinterpret_cast<const float4*>(ks + jj * D + d);
       if constexpr (G == 1) {
         const float dv = dsb[b][jj][0];
-        acc[0] = f2fma(pk2(dv, dv), pk2(kk.x, kk.y), acc[0]);
+        const uint64_t d2 = pk2(dv, dv);
+        acc[0] = f2fma(d2, pk2(kk.x, kk.y), acc[0]);
+        acc[1] = f2fma(d2, pk2(kk.z, kk.w), acc[1]);
       } else {
-        const uint64_t k0 = pk2(kk.x, kk.x), k1 = pk2(kk.y, kk.y);
+        const uint64_t kd[4] = {pk2(kk.x, kk.x), pk2(kk.y, kk.y), pk2(kk.z, kk.z), pk2(kk.w, kk.w)};
+        uint64_t w2[G / 2];
         if constexpr (G == 2) {
-          const uint64_t t = *reinterpret_cast<const uint64_t*>(&dsb[b][jj][0]);
-          acc[0] = f2fma(t, k0, acc[0]);
-          acc[1] = f2fma(t, k1, acc[1]);
+          w2[0] = *reinterpret_cast<const uint64_t*>(&dsb[b][jj][0]);
         } else {
 #pragma unroll
           for (int hp = 0; hp < G / 2; hp += 2) {
             const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(&dsb[b][jj][2 * hp]);
-            acc[hp] = f2fma(t.x, k0, acc[hp]);
-            acc[G / 2 + hp] = f2fma(t.x, k1, acc[G / 2 + hp]);
-            acc[hp + 1] = f2fma(t.y, k0, acc[hp + 1]);
-            acc[G / 2 + hp + 1] = f2fma(t.y, k1, acc[G / 2 + hp + 1]);
+            w2[hp] = t.x, w2[hp + 1] = t.y;
           }
         }
+#pragma unroll
+        for (int i = 0; i < DPT; ++i)
+#pragma unroll
+          for (int hp = 0; hp < G / 2; ++hp)
+            acc[i * (G / 2) + hp] = f2fma(w2[hp], kd[i], acc[i * (G / 2) + hp]);
       }
     };
     if (rows == CH) {
@@ -597,7 +646,10 @@ __global__ void __launch_bounds__(32 + DecCfg<D, G>::P2T, 1)
       for (int jj = kg; jj < rows; jj += KG2) key_dq(jj);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) {
+      mbar_arrive(&empty[s]);
+      mbar_arrive(&ds_empty[b]);
+    }
     if (++lc == a.cpp) lc = 0, ++pair;
   }
   if (ok && seg >= 0) finish();
@@ -633,7 +685,7 @@ cudaError_t decode_impl(const DecArgs& a, cudaStream_t stream) {
   k1<<<a.grid, 32 * (1 + C::P1W), C::SMEM1, stream>>>(tm_v, tm_p, tm_s, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2<<<a.grid, 32 + C::P2T, C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
+  k2<<<a.grid, 32 * (2 + C::P2W), C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
   return cudaGetLastError();
 }
 
