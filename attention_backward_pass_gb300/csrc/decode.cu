@@ -46,7 +46,7 @@ namespace attnbwd {
 
 namespace {
 
-constexpr int kDecChunk = 32;                 // keys per chunk
+constexpr int kDecChunk = 64;                 // keys per chunk
 constexpr int kDecSmsFallback = 152;
 
 struct DecArgs {
@@ -176,16 +176,17 @@ struct DecCfg {
   // decode_dq: stage = [K rows [CH][D] | parked probs*dp | probs]
   static constexpr int P2W = 8;                           // accumulating warps
   static constexpr int P2T = 32 * P2W;
-  static constexpr int DPT = 4;                           // d per accumulating thread
+  static constexpr int DPT = G <= 8 ? 8 : 4;              // d per accumulating thread
   static constexpr int KG2 = P2T * DPT / D;               // key groups
   static constexpr int NB = 4;                            // d_scores buffers
-  static constexpr int DSB_BYTES = NB * CH * G * 4;
+  static constexpr int DSW = 2;                           // d_scores warps
+  static constexpr int DSB_BYTES = NB * CH * G * 4 + G * D * 4;  // d_scores ring, d_q reduction
   static constexpr int NS2 = dec_clamp((kDecSmemMax - 2048 - DSB_BYTES) / STAGE, 2, 12);
   static constexpr int SMEM2 = NS2 * STAGE + 128;
-  static constexpr int SLOT2 = KG2 * G * D;               // d_q[KG2][G][D]
+  static constexpr int SLOT2 = G * D;                     // d_q[G][D]
   static_assert(HPW * DPL <= 64 && G % HPW == 0 && KG >= 1 && CH % KG == 0 && D % 64 == 0 &&
                     D <= 256, "decode_dp split");
-  static_assert(KG2 >= 1 && CH % KG2 == 0, "decode_dq split");
+  static_assert(KG2 >= 1 && CH % KG2 == 0 && CH % 32 == 0, "decode_dq split");
   static_assert(SMEM1 + 1024 <= kDecSmemMax && SMEM2 + DSB_BYTES + 1024 <= kDecSmemMax,
                 "decode shared memory");
 };
@@ -337,10 +338,9 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
   float dout[HPW][DPL];
   float sumpd = 0.f;
   int cur_pair = -1, seg = -1;
-  int pair = pair0, lc = lc0;
+  int pair = pair0, lc = lc0, seq = pair0 / a.n_kv, kv = pair0 % a.n_kv;
   bool ok = true;
   for (int c = 0; c < nch; ++c) {
-    const int seq = pair / a.n_kv, kv = pair % a.n_kv;
     const int j0 = lc * CH, rows = min(CH, a.hist - j0);
     const int h_own = kv * G + hg * HPW + g_own;  // query head of this lane's sums
     if (pair != cur_pair) {
@@ -410,29 +410,34 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
     if (a.side_tma) fence_proxy_async_smem();  // the staging array is read by a tensor store
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (++lc == a.cpp) lc = 0, ++pair;
+    if (++lc == a.cpp) {
+      lc = 0, ++pair;
+      if (++kv == a.n_kv) kv = 0, ++seq;
+    }
   }
   if (ok && seg >= 0 && owner) slots[(size_t)seg * C::SLOT1 + kgp * G + hg * HPW + g_own] = sumpd;
 }
 
 // --------------------------------------------------------------- decode_dq
 // tm_k: K as {D, n_kv, hist, seqs}, boxes {D, 1, CH, 1}.
-// Warps: 0 producer; 1 .. P2W accumulate d_q (P2T threads, DPT = 4 d each,
-// KG2 key groups); P2W + 1 forms each chunk's d_scores into a ring of NB
-// shared buffers, one chunk ahead of the accumulating warps.
+// Warps: 0 producer; 1 .. P2W accumulate d_q (P2T threads, DPT d each, KG2
+// key groups); the last DSW warps form each chunk's d_scores (each warp every
+// DSW-th head) into a ring of NB shared buffers, ahead of the accumulating
+// warps.
 template <int D, int G>
-__global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
+__global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DSW), 1)
     decode_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_p,
                      const __grid_constant__ CUtensorMap tm_s, const DecArgs a) {
   using C = DecCfg<D, G>;
   constexpr int CH = C::CH, NS = C::NS2, NB = C::NB, P2T = C::P2T, P2W = C::P2W, KG2 = C::KG2;
-  constexpr int DPT = C::DPT;
+  constexpr int DPT = C::DPT, DSW = C::DSW;
   constexpr int NACC = G == 1 ? DPT / 2 : DPT * (G / 2);  // packed accumulators
   extern __shared__ uint8_t smem_raw[];
   // [NS][K rows [CH][D] | parked probs * dp [G][CH] | probs [G][CH]], 128-byte aligned
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   __shared__ __align__(16) float dsb[NB][CH][G];  // chunks' d_scores, key-major
+  __shared__ __align__(16) float red[G * D];      // the CTA's d_q partial of a segment
   __shared__ int last_s;
   __shared__ __align__(8) uint64_t full[NS], empty[NS], ds_full[NB], ds_empty[NB];
 
@@ -445,10 +450,10 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], P2W + 1);
+      mbar_init(&empty[s], P2W + DSW);
     }
     for (int b = 0; b < NB; ++b) {
-      mbar_init(&ds_full[b], 32);
+      mbar_init(&ds_full[b], 32 * DSW);
       mbar_init(&ds_empty[b], P2W);
     }
     fence_barrier_init();
@@ -486,29 +491,34 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
     return;
   }
 
-  if (warp == 1 + P2W) {
-    // ------------------------------------------------------- d_scores warp
-    // lane j = key j of the chunk: d_scores = probs*dp - probs * sum_pd for
-    // every head, stored to global memory and to dsb
+  if (warp > P2W) {
+    // ------------------------------------------------------ d_scores warps
+    // lane j = keys j, j + 32, .. of the chunk: d_scores = probs*dp - probs * sum_pd for
+    // heads dw, dw + DSW, ..., stored to global memory and to dsb
+    const int dw = warp - 1 - P2W;
     float sp[G];  // sum_pd of the current pair, every head
     int cur = -1;
-    int pair = pair0, lc = lc0;
+    int pair = pair0, lc = lc0, seq = pair0 / a.n_kv, kv = pair0 % a.n_kv;
     for (int c = 0; c < nch; ++c) {
-      const int seq = pair / a.n_kv, kv = pair % a.n_kv;
       const int j0 = lc * CH, rows = min(CH, a.hist - j0);
-      if (pair != cur) {  // sum_pd of the pair from decode_dp's partials
+      if (pair != cur) {
+        // sum_pd of the pair from decode_dp's partials: the lanes load the
+        // (CTA, key group, head) terms side by side, lane l only terms of
+        // head l % G, then lanes of equal l % G are summed
         cur = pair;
+        const long long fa = (long long)pair * a.cpp;
+        const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+        const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+        const int nt = (ib - ia + 1) * C::SLOT1;
         float v = 0.f;
-        if (lane < G) {
-          const long long fa = (long long)pair * a.cpp;
-          const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
-          const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
-          for (int i = ia; i <= ib; ++i) {
-            const int sg = pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
-            const float* p1 = a.part1 + ((size_t)i * a.max_seg + sg) * C::SLOT1;
-            for (int q = 0; q < C::KG; ++q) v += p1[q * G + lane];
-          }
+#pragma unroll 4
+        for (int t = lane; t < nt; t += 32) {
+          const int i = ia + t / C::SLOT1;
+          const int sg = pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
+          v += a.part1[((size_t)i * a.max_seg + sg) * C::SLOT1 + t % C::SLOT1];
         }
+#pragma unroll
+        for (int off = 16; off >= G; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
 #pragma unroll
         for (int g = 0; g < G; ++g) sp[g] = __shfl_sync(0xffffffffu, v, g);
       }
@@ -518,37 +528,48 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
       if (__any_sync(0xffffffffu, !ok)) break;
       const float* wsd = reinterpret_cast<const float*>(smem + s * C::STAGE + C::ROWS_BYTES);
       const float* psd = wsd + C::SIDE;
-      const bool in = lane < rows;
-      const size_t gi0 = ((size_t)seq * a.n_heads + kv * G) * a.hist + j0 + lane;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float w, pv;
-        if (a.side_tma) {
-          w = wsd[g * CH + lane];
-          pv = psd[g * CH + lane];
-        } else {
-          w = in ? a.d_scores[gi0 + (size_t)g * a.hist] : 0.f;
-          pv = in ? __ldg(a.probs + gi0 + (size_t)g * a.hist) : 0.f;
+      for (int r = 0; r < CH / 32; ++r) {
+        const int jl = lane + 32 * r;  // key of the chunk
+        const bool in = jl < rows;
+        const size_t gi0 = ((size_t)seq * a.n_heads + kv * G) * a.hist + j0 + jl;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          if (g % DSW != dw) continue;
+          float w, pv;
+          if (a.side_tma) {
+            w = wsd[g * CH + jl];
+            pv = psd[g * CH + jl];
+          } else {
+            w = in ? a.d_scores[gi0 + (size_t)g * a.hist] : 0.f;
+            pv = in ? __ldg(a.probs + gi0 + (size_t)g * a.hist) : 0.f;
+          }
+          const float ds = fmaf(-pv, sp[g], w);
+          if (in) a.d_scores[gi0 + (size_t)g * a.hist] = ds;
+          dsb[b][jl][g] = ds;
         }
-        const float ds = fmaf(-pv, sp[g], w);
-        if (in) a.d_scores[gi0 + (size_t)g * a.hist] = ds;
-        dsb[b][lane][g] = ds;
       }
       mbar_arrive(&ds_full[b]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (++lc == a.cpp) lc = 0, ++pair;
+      if (++lc == a.cpp) {
+        lc = 0, ++pair;
+        if (++kv == a.n_kv) kv = 0, ++seq;
+      }
     }
     return;
   }
 
   // -------------------------------------------------------- accumulators
-  // thread t2 owns d .. d + 3 for the keys kg, kg + KG2, ... of every chunk.
-  // For even G the packed accumulators pair consecutive heads:
-  // acc[i (G/2) + hp] = (d_q[2hp][d + i], d_q[2hp+1][d + i]); for G = 1,
-  // acc[i] = (d_q[0][d + 2i], d_q[0][d + 2i + 1]).
+  // Thread t2 (key group kg, index tk within it) owns DPT head-dim elements:
+  // dd(i) = 4 tk + i for i < 4 and, when DPT = 8, D / 2 + 4 tk + i - 4 (two
+  // 16-byte pieces, so a warp's loads cover contiguous runs), for the keys kg,
+  // kg + KG2, ... of every chunk.  For even G the packed accumulators pair
+  // consecutive heads: acc[i (G/2) + hp] = (d_q[2hp][dd(i)], d_q[2hp+1][dd(i)]);
+  // for G = 1, acc[i] = (d_q[0][dd(2i)], d_q[0][dd(2i+1)]).
   const int t2 = threadIdx.x - 32;
-  const int kg = t2 / (D / DPT), d = DPT * (t2 % (D / DPT));
+  const int kg = t2 / (D / DPT), tk = t2 % (D / DPT);
+  auto dd = [&](int i) { return i < 4 ? 4 * tk + i : D / 2 + 4 * tk + i - 4; };
   float* slots = a.part2 + (size_t)blockIdx.x * a.max_seg * C::SLOT2;
   uint64_t acc[NACC];
 #pragma unroll
@@ -556,7 +577,9 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
   int cur_pair = -1, seg = -1;
   bool ok = true;
 
-  // segment `seg` (pair cur_pair) is complete in this CTA
+  // segment `seg` (pair cur_pair) is complete in this CTA: sum the key
+  // groups in shared memory (in key-group order), write the CTA's partial,
+  // and let the last CTA of the pair sum the partials in CTA order
   auto finish = [&]() {
     float x[G][DPT];
     if constexpr (G == 1) {
@@ -568,12 +591,28 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
 #pragma unroll
         for (int hp = 0; hp < G / 2; ++hp) up2(acc[i * (G / 2) + hp], x[2 * hp][i], x[2 * hp + 1][i]);
     }
-    float* sl = slots + (size_t)seg * C::SLOT2 + (size_t)kg * G * D;
+    for (int r = 0; r < KG2; ++r) {
+      if (kg == r) {
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      *reinterpret_cast<float4*>(sl + g * D + d) = make_float4(x[g][0], x[g][1], x[g][2], x[g][3]);
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int q = 0; q < DPT / 4; ++q) {
+            float4* dst = reinterpret_cast<float4*>(red + g * D + dd(4 * q));
+            float4 v = make_float4(x[g][4 * q], x[g][4 * q + 1], x[g][4 * q + 2], x[g][4 * q + 3]);
+            if (r > 0) {
+              const float4 o = *dst;
+              v.x += o.x, v.y += o.y, v.z += o.z, v.w += o.w;
+            }
+            *dst = v;
+          }
+      }
+      named_bar_sync(1, P2T);
+    }
+    float* sl = slots + (size_t)seg * C::SLOT2;
+    for (int o = 4 * t2; o < G * D; o += 4 * P2T)
+      *reinterpret_cast<float4*>(sl + o) = *reinterpret_cast<const float4*>(red + o);
     __threadfence();
-    named_bar_sync(1, P2T);
+    named_bar_sync(1, P2T);  // every partial written; red may be reused
     const long long fa = (long long)cur_pair * a.cpp;
     const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
     const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
@@ -584,14 +623,12 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
       __threadfence();
       const int seq = cur_pair / a.n_kv, kv = cur_pair % a.n_kv;
       for (int o = t2; o < G * D; o += P2T) {
-        const int g = o / D, dd = o % D;
         float t = 0.f;
         for (int i = ia; i <= ib; ++i) {
           const int sg = cur_pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
-          const float* p2 = a.part2 + ((size_t)i * a.max_seg + sg) * C::SLOT2 + g * D + dd;
-          for (int q = 0; q < KG2; ++q) t += __ldcg(p2 + (size_t)q * G * D);
+          t += __ldcg(a.part2 + ((size_t)i * a.max_seg + sg) * C::SLOT2 + o);
         }
-        a.d_q[((size_t)seq * a.n_heads + kv * G + g) * D + dd] = t;
+        a.d_q[((size_t)seq * a.n_heads + kv * G) * D + o] = t;
       }
     }
   };
@@ -614,14 +651,18 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
     }
     const float* ks = reinterpret_cast<const float*>(smem + s * C::STAGE);
     auto key_dq = [&](int jj) {
-      const float4 kk = *reinterpret_cast<const float4*>(ks + jj * D + d);
+      float kk[DPT];
+#pragma unroll
+      for (int q = 0; q < DPT / 4; ++q) {
+        const float4 t = *reinterpret_cast<const float4*>(ks + jj * D + dd(4 * q));
+        kk[4 * q] = t.x, kk[4 * q + 1] = t.y, kk[4 * q + 2] = t.z, kk[4 * q + 3] = t.w;
+      }
       if constexpr (G == 1) {
         const float dv = dsb[b][jj][0];
         const uint64_t d2 = pk2(dv, dv);
-        acc[0] = f2fma(d2, pk2(kk.x, kk.y), acc[0]);
-        acc[1] = f2fma(d2, pk2(kk.z, kk.w), acc[1]);
+#pragma unroll
+        for (int i = 0; i < DPT / 2; ++i) acc[i] = f2fma(d2, pk2(kk[2 * i], kk[2 * i + 1]), acc[i]);
       } else {
-        const uint64_t kd[4] = {pk2(kk.x, kk.x), pk2(kk.y, kk.y), pk2(kk.z, kk.z), pk2(kk.w, kk.w)};
         uint64_t w2[G / 2];
         if constexpr (G == 2) {
           w2[0] = *reinterpret_cast<const uint64_t*>(&dsb[b][jj][0]);
@@ -633,10 +674,12 @@ __global__ void __launch_bounds__(32 * (2 + DecCfg<D, G>::P2W), 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < DPT; ++i)
+        for (int i = 0; i < DPT; ++i) {
+          const uint64_t kd = pk2(kk[i], kk[i]);
 #pragma unroll
           for (int hp = 0; hp < G / 2; ++hp)
-            acc[i * (G / 2) + hp] = f2fma(w2[hp], kd[i], acc[i * (G / 2) + hp]);
+            acc[i * (G / 2) + hp] = f2fma(w2[hp], kd, acc[i * (G / 2) + hp]);
+        }
       }
     };
     if (rows == CH) {
@@ -685,7 +728,7 @@ cudaError_t decode_impl(const DecArgs& a, cudaStream_t stream) {
   k1<<<a.grid, 32 * (1 + C::P1W), C::SMEM1, stream>>>(tm_v, tm_p, tm_s, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2<<<a.grid, 32 * (2 + C::P2W), C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
+  k2<<<a.grid, 32 * (1 + C::P2W + C::DSW), C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
   return cudaGetLastError();
 }
 
