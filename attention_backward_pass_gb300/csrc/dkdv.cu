@@ -127,8 +127,12 @@ struct Layout {
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
   static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
-  static constexpr int OFF_BAR = OFF_STG + BM * STG_D * 4;
-  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 3 * NSB + 2 + PB + 7;
+  // dropout keep bits of two query tiles, [2][BN keys][BM / 16] x 16 bits,
+  // drawn by the dQ warps one tile ahead of the softmax warps
+  static constexpr int NCH = BM / 16;
+  static constexpr int OFF_BITS = OFF_STG + BM * STG_D * 4;
+  static constexpr int OFF_BAR = OFF_BITS + 2 * BN * NCH * 2;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
@@ -427,6 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* final_bar = kv_full + 4;         // unwinding: products in flight done
   uint64_t* v_ready = kv_full + 5;           // (VTM) V copied into tensor memory
   uint64_t* pfree = kv_full + 6;             // [NSB] (INPL) GEMM3/4 done with buffer b
+  uint64_t* bits_full = pfree + NSB;         // [2] dropout keep bits of a tile drawn (by parity)
+  uint16_t* bits_s = reinterpret_cast<uint16_t*>(smem + L::OFF_BITS);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
   constexpr int RST = L::ROW_ST;
 
@@ -462,6 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(final_bar, 1);
     mbar_init(v_ready, kSoftmaxThreads);
     for (int s = 0; s < NSB; ++s) mbar_init(&pfree[s], 1);
+    mbar_init(&bits_full[0], kDqThreads);
+    mbar_init(&bits_full[1], kDqThreads);
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -776,7 +784,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + rs * BM * 4);
       const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + rs * BM * 4);
-      const uint32_t bh = (uint32_t)(w.b * a.H + h);
       const bool plain = tile_is_plain(a, q0, BM, w.k0, BN);
       const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
       const uint32_t t_p = L::INPL ? t_s : tmem + lane_base + L::T_P + pb * L::PCOLS;
@@ -786,6 +793,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dsn_base = smem_u32(
           smem + (L::INPL ? L::OFF_Q + (t % NAT) * L::NAT_STRIDE : L::OFF_DSN + pb * L::P_BYTES));
       const uint32_t dsn_tile = dsn_lane + dsn_base;
+      // dropout: this tile's keep bits, drawn by the dQ warps
+      if (a.dropout && !warp_wait(&bits_full[t & 1], (t >> 1) & 1, a.err)) {
+        ok = false;
+        break;
+      }
+      const uint16_t* kbits = bits_s + ((t & 1) * BN + jj) * L::NCH;
       if (L::INPL && !a.has_mask && !a.dropout) {
         softmax_frag(a, t_s + cbeg, t_dp + cbeg, sLSE + cbeg, sDelta + cbeg, plain, q0 + cbeg,
                      w.k0 + quad * 32, key_ok4, dsn_base + dsn_frag, xo2);
@@ -844,22 +857,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               // additive mask and / or dropout: per-pair exponent addend
               // (-inf for invisible or hard-masked pairs) and multiplier, then
-              // the same packed arithmetic as above.  The chunk's four Philox
-              // calls (one per four consecutive queries of this key) become a
-              // 16-bit keep mask first, and its 16 mask values are loaded
-              // together from in-range addresses, so the loads overlap.
-              uint32_t keep_bits = 0xffffu;
-              if (a.dropout) {
-                keep_bits = 0u;
-#pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                  const Philox4 r = philox4x32_10((uint32_t)(q0 + c0 + 4 * g4) >> 2, (uint32_t)kj,
-                                                  bh, 0u, a.seed_lo, a.seed_hi);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    keep_bits |= (r.w[e] >= a.drop_threshold ? 1u : 0u) << (4 * g4 + e);
-                }
-              }
+              // the same packed arithmetic as above.  The chunk's dropout keep
+              // mask (16 bits, one per query) was drawn by the dQ warps, and
+              // its 16 mask values are loaded together from in-range
+              // addresses, so the loads overlap.
+              const uint32_t keep_bits = a.dropout ? (uint32_t)kbits[c0 / 16] : 0xffffu;
               float mv[16];
               if (a.has_mask) {
                 const float* mr = a.mask + w.b * a.msb + h * a.msh +
@@ -1025,7 +1027,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     float* stg = reinterpret_cast<float*>(smem + L::OFF_STG);
     const long long rstride = a.layout == 0 ? D : (long long)a.H * D;
+    // dropout keep bits of tile tt into buffer tt & 1: for key row jr and
+    // 16-query chunk ci, bit 4 g4 + e keeps query q0 + 16 ci + 4 g4 + e (one
+    // Philox4x32-10 call per four consecutive queries of a key)
+    auto draw_bits = [&](int tt) {
+      const int h2 = w.kvh * a.group + tt / w.tiles_per_head;
+      const int q02 = w.q_first + (tt % w.tiles_per_head) * BM;
+      const uint32_t bh2 = (uint32_t)(w.b * a.H + h2);
+      uint16_t* dst = bits_s + (tt & 1) * BN * L::NCH;
+      for (int jr = tid; jr < BN; jr += kDqThreads) {
+#pragma unroll 1
+        for (int ci = 0; ci < L::NCH; ++ci) {
+          uint32_t kb = 0u;
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const Philox4 r = philox4x32_10((uint32_t)(q02 + 16 * ci + 4 * g4) >> 2,
+                                            (uint32_t)(w.k0 + jr), bh2, 0u, a.seed_lo, a.seed_hi);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kb |= (r.w[e] >= a.drop_threshold ? 1u : 0u) << (4 * g4 + e);
+          }
+          dst[jr * L::NCH + ci] = (uint16_t)kb;
+        }
+      }
+      mbar_arrive(&bits_full[tt & 1]);
+    };
+    // tile t + 1's buffer was last read by the softmax of tile t - 1, which
+    // finished before GEMM5 of t - 1 (waited for in the previous iteration)
+    if (a.dropout && T > 0) draw_bits(0);
     for (int t = 0; t < T; ++t) {
+      if (a.dropout && t + 1 < T) draw_bits(t + 1);
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
