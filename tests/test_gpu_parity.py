@@ -54,6 +54,29 @@ def test_small_parity(name, dtype):
     assert all(e <= TOL[dtype] for e in errs.values()), errs
 
 
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("kind", ["dense", "partial"])
+def test_real_valued_mask(kind, dtype):
+    """An additive mask with arbitrary finite values (N(0,1)) besides the
+    hard-mask sentinel.  "partial" keeps real values only for the first 96
+    queries, so that some query tiles of a key tile have only 0 / -1e30 entries
+    and others do not."""
+    from oracle import attention as OA
+    p = P(seq_q=256, seq_k=300, causal=1, causal_offset=100, has_mask=1, dropout_prob=0.1,
+          seed=0x5EED0005)
+    p.dtype = dtype
+    Q, K, V, dO, mask = W.make_inputs(p, 4321)
+    real = np.random.default_rng(77).standard_normal(mask.shape).astype(np.float32)
+    if kind == "partial":
+        real[:, :, 96:, :] = 0.0
+    mask = np.where(mask < -1.0e29, mask, real).astype(np.float32)
+    O, LSE = OA.forward(p, Q, K, V, mask)
+    case = dict(Q=Q, K=K, V=V, dO=dO, mask=mask, O=W.round_io(O.astype(np.float32), p.dtype),
+                LSE=LSE.astype(np.float32))
+    errs = compare(p, case)
+    assert all(e <= TOL[dtype] for e in errs.values()), errs
+
+
 def test_keep_mask_bit_exact():
     import torch
     import attention_backward_pass_gb300 as ab
