@@ -174,9 +174,9 @@ struct DecCfg {
   static constexpr int SMEM1 = NS1 * STAGE + 128;             // + alignment slack
   static constexpr int SLOT1 = KG * G;                        // sum_pd[KG][G]
   // decode_dq: stage = [K rows [CH][D] | parked probs*dp | probs]
-  static constexpr int P2W = 8;                           // accumulating warps
+  static constexpr int P2W = G <= 8 ? 16 : 8;             // accumulating warps
   static constexpr int P2T = 32 * P2W;
-  static constexpr int DPT = G <= 8 ? 8 : 4;              // d per accumulating thread
+  static constexpr int DPT = 4;                           // d per accumulating thread
   static constexpr int KG2 = P2T * DPT / D;               // key groups
   static constexpr int NB = 4;                            // d_scores buffers
   static constexpr int DSW = 2;                           // d_scores warps
