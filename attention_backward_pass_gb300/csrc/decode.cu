@@ -260,6 +260,9 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P1W), 1)
 
   if (blockIdx.x == 0)  // decode_dq's per-pair completion counters
     for (int i = threadIdx.x; i < a.n_pairs; i += blockDim.x) a.count[i] = 0u;
+  // decode_dq may start its CTAs (and stream K) as SMs free up; it waits for
+  // this grid before it reads anything written here
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -465,6 +468,11 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
     if (lane == 0) {
       int issued = 0;
       int pair = pair0, lc = lc0;  // chunk c
+      // The first NS chunks' K rows and probs are requested before the d_p
+      // pass has finished; their parked probs*dp slices (written by it) only
+      // after griddep_wait.
+      int pre_seq[NS], pre_kv[NS], pre_j0[NS];
+      const int pre = nch < NS ? nch : NS;
       for (int c = 0; c < nch; ++c) {
         const int s = c % NS;
         if (c >= NS && !mbar_wait(&empty[s], ((c / NS) - 1) & 1, a.err)) break;
@@ -475,11 +483,23 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
         mbar_expect_tx(&full[s], C::ROWS_BYTES + (a.side_tma ? 2u * C::SIDE * 4u : 0u));
         tma_load_4d(st, &tm_k, &full[s], 0, kv, j0, seq);
         if (a.side_tma) {
-          tma_load_3d(st + C::ROWS_BYTES, &tm_s, &full[s], j0, kv * G, seq);
           tma_load_3d(st + C::ROWS_BYTES + C::SIDE * 4, &tm_p, &full[s], j0, kv * G, seq);
+          if (c < pre) {
+            pre_seq[c] = seq, pre_kv[c] = kv, pre_j0[c] = j0;
+          } else {
+            tma_load_3d(st + C::ROWS_BYTES, &tm_s, &full[s], j0, kv * G, seq);
+          }
         }
         issued = c + 1;
+        if (c + 1 == pre) {
+          griddep_wait();
+          if (a.side_tma)
+            for (int i = 0; i < pre; ++i)
+              tma_load_3d(smem + i * C::STAGE + C::ROWS_BYTES, &tm_s, &full[i], pre_j0[i],
+                          pre_kv[i] * G, pre_seq[i]);
+        }
       }
+      if (issued < pre) griddep_wait();  // (left early on an error)
       // copies still in flight land before the CTA exits
       for (int c = issued > NS ? issued - NS : 0; c < issued; ++c) {
         const long long t0 = clock64();
@@ -496,6 +516,7 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
     // lane j = keys j, j + 32, .. of the chunk: d_scores = probs*dp - probs * sum_pd for
     // heads dw, dw + DSW, ..., stored to global memory and to dsb
     const int dw = warp - 1 - P2W;
+    griddep_wait();  // sum_pd partials and parked values come from decode_dp
     float sp[G];  // sum_pd of the current pair, every head
     int cur = -1;
     int pair = pair0, lc = lc0, seq = pair0 / a.n_kv, kv = pair0 % a.n_kv;
@@ -567,6 +588,7 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
   // kg + KG2, ... of every chunk.  For even G the packed accumulators pair
   // consecutive heads: acc[i (G/2) + hp] = (d_q[2hp][dd(i)], d_q[2hp+1][dd(i)]);
   // for G = 1, acc[i] = (d_q[0][dd(2i)], d_q[0][dd(2i+1)]).
+  griddep_wait();  // the pair counters are zeroed by decode_dp
   const int t2 = threadIdx.x - 32;
   const int kg = t2 / (D / DPT), tk = t2 % (D / DPT);
   auto dd = [&](int i) { return i < 4 ? 4 * tk + i : D / 2 + 4 * tk + i - 4; };
@@ -728,7 +750,20 @@ cudaError_t decode_impl(const DecArgs& a, cudaStream_t stream) {
   k1<<<a.grid, 32 * (1 + C::P1W), C::SMEM1, stream>>>(tm_v, tm_p, tm_s, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2<<<a.grid, 32 * (1 + C::P2W + C::DSW), C::SMEM2, stream>>>(tm_k, tm_p, tm_s, a);
+  // decode_dq may begin while decode_dp finishes (programmatic dependent
+  // launch); it synchronises with griddep_wait before using dp's outputs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(32 * (1 + C::P2W + C::DSW));
+  cfg.dynamicSmemBytes = C::SMEM2;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k2, tm_k, tm_p, tm_s, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

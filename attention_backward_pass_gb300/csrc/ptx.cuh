@@ -121,6 +121,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
       : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream (launched
+// with programmatic stream serialization) start its CTAs; and, in that
+// kernel, wait until the preceding one has completed with its memory
+// operations visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 3-D tiled load / store, as the 2-D forms.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
                                             int c1, int c2) {
