@@ -127,11 +127,13 @@ struct Layout {
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
   static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
-  // dropout keep bits of two query tiles, [2][BN keys][BM / 16] x 16 bits,
-  // drawn by the dQ warps one tile ahead of the softmax warps
+  // (fp32, D=64) dropout keep bits of two query tiles, [2][BN keys][BM / 16]
+  // x 16 bits, drawn by the dQ warps one tile ahead of the softmax warps; the
+  // other configurations draw them in the softmax warps
+  static constexpr bool DBITS = !BF16 && D == 64;
   static constexpr int NCH = BM / 16;
   static constexpr int OFF_BITS = OFF_STG + BM * STG_D * 4;
-  static constexpr int OFF_BAR = OFF_BITS + 2 * BN * NCH * 2;
+  static constexpr int OFF_BAR = OFF_BITS + (DBITS ? 2 * BN * NCH * 2 : 0);
   static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
@@ -794,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           smem + (L::INPL ? L::OFF_Q + (t % NAT) * L::NAT_STRIDE : L::OFF_DSN + pb * L::P_BYTES));
       const uint32_t dsn_tile = dsn_lane + dsn_base;
       // dropout: this tile's keep bits, drawn by the dQ warps
-      if (a.dropout && !warp_wait(&bits_full[t & 1], (t >> 1) & 1, a.err)) {
+      if (L::DBITS && a.dropout && !warp_wait(&bits_full[t & 1], (t >> 1) & 1, a.err)) {
         ok = false;
         break;
       }
@@ -858,10 +860,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // additive mask and / or dropout: per-pair exponent addend
               // (-inf for invisible or hard-masked pairs) and multiplier, then
               // the same packed arithmetic as above.  The chunk's dropout keep
-              // mask (16 bits, one per query) was drawn by the dQ warps, and
-              // its 16 mask values are loaded together from in-range
-              // addresses, so the loads overlap.
-              const uint32_t keep_bits = a.dropout ? (uint32_t)kbits[c0 / 16] : 0xffffu;
+              // mask (16 bits, one per query) was drawn by the dQ warps (fp32,
+              // D=64) or is drawn here first (four Philox calls, one per four
+              // consecutive queries of this key), and its 16 mask values are
+              // loaded together from in-range addresses, so the loads overlap.
+              uint32_t keep_bits = 0xffffu;
+              if constexpr (L::DBITS) {
+                if (a.dropout) keep_bits = kbits[c0 / 16];
+              } else if (a.dropout) {
+                keep_bits = 0u;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                  const Philox4 r = philox4x32_10((uint32_t)(q0 + c0 + 4 * g4) >> 2, (uint32_t)kj,
+                                                  (uint32_t)(w.b * a.H + h), 0u, a.seed_lo,
+                                                  a.seed_hi);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    keep_bits |= (r.w[e] >= a.drop_threshold ? 1u : 0u) << (4 * g4 + e);
+                }
+              }
               float mv[16];
               if (a.has_mask) {
                 const float* mr = a.mask + w.b * a.msb + h * a.msh +
@@ -1053,9 +1070,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // tile t + 1's buffer was last read by the softmax of tile t - 1, which
     // finished before GEMM5 of t - 1 (waited for in the previous iteration)
-    if (a.dropout && T > 0) draw_bits(0);
+    if constexpr (L::DBITS) {
+      if (a.dropout && T > 0) draw_bits(0);
+    }
     for (int t = 0; t < T; ++t) {
-      if (a.dropout && t + 1 < T) draw_bits(t + 1);
+      if constexpr (L::DBITS) {
+        if (a.dropout && t + 1 < T) draw_bits(t + 1);
+      }
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
