@@ -123,6 +123,11 @@ DECODE = {
     "g2_kv2_d64_ragged": W.DecodeProblem(3, 4, 2, 64, 17),
     "g1_d128": W.DecodeProblem(2, 4, 4, 128, 1000),
     "g16_d64": W.DecodeProblem(1, 16, 1, 64, 77),
+    # many short sequences: CTAs cover several (sequence, KV head) pairs
+    "many_seqs_g4_kv2_d128": W.DecodeProblem(300, 8, 2, 128, 100),
+    "many_seqs_g2_kv4_d64_odd": W.DecodeProblem(260, 8, 4, 64, 37),
+    # few long sequences: each pair is split over many CTAs
+    "long_g8_d256": W.DecodeProblem(3, 8, 1, 256, 20000),
 }
 
 
