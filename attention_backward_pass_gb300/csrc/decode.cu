@@ -29,12 +29,17 @@
 //     shuffle-adds (no selects); one lane per head ends with the head's dp.
 //     probs*dp goes to a staging array of the stage, which the producer
 //     writes back with one tensor store when it recycles the stage.
-//   decode_dq compute threads: two d per thread, KG2 key groups.  Per chunk
-//     the threads first form the chunk's G x CH d_scores (coalesced stores,
-//     a copy kept in shared memory), then accumulate d_q.  The partial d_q of
-//     a segment goes to the workspace; the last CTA of a pair to finish (a
-//     counter in the workspace, zeroed by decode_dp) sums the partials in CTA
-//     order and writes d_q, so the result does not depend on timing.
+//   decode_dq: two warps form the chunk's G x CH d_scores (coalesced stores,
+//     a copy in a small shared ring) ahead of 16 accumulating warps (8 when a
+//     KV head serves 16 query heads; four
+//     d per thread, KG2 key groups) that add d_q.  The partial d_q of a
+//     segment is summed over the key groups in shared memory and written to
+//     the workspace; the last CTA of a pair to finish (a counter in the
+//     workspace, zeroed by decode_dp) sums the partials in CTA order and
+//     writes d_q, so the result does not depend on timing.  decode_dq is a
+//     programmatic dependent of decode_dp: its producer streams the first K
+//     chunks while decode_dp finishes, and everything that reads decode_dp's
+//     outputs waits for it first (griddepcontrol.wait).
 #include <cuda_runtime.h>
 
 #include <cstring>
