@@ -149,13 +149,26 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&x)[G], int lane) {
   return r;
 }
 
-// Chunk range [f0, f1) of CTA i; the CTA that owns chunk f.
+// Chunk range [f0, f1) of CTA i; the CTA that owns chunk f.  32-bit
+// arithmetic whenever the products fit (a 64-bit division is a long software
+// sequence on the GPU, and these run inside the kernels' segment changes).
 __host__ __device__ __forceinline__ long long dec_begin(long long i, long long n, int grid) {
+  if (n * grid < (1LL << 32)) return (long long)((uint32_t)(i * n) / (uint32_t)grid);
   return i * n / grid;
 }
 __host__ __device__ __forceinline__ int dec_cta_of(long long f, long long n, int grid) {
+  if ((f + 1) * grid + n < (1LL << 32))
+    return (int)(((uint32_t)((f + 1) * grid) + (uint32_t)n - 1u) / (uint32_t)n) - 1;
   return (int)(((f + 1) * grid + n - 1) / n - 1);
 }
+
+// The (sequence, KV head) pair of CTA i's first chunk (cpp chunks per pair).
+__device__ __forceinline__ int dec_pair0(int i, long long n, int grid, int cpp) {
+  const long long f = dec_begin(i, n, grid);
+  return n < (1LL << 31) ? (int)((uint32_t)f / (uint32_t)cpp) : (int)(f / cpp);
+}
+
+constexpr int kDecDefer = 8;  // d_q segments whose completion the accumulators defer
 
 constexpr int kDecSmemMax = 227 * 1024;  // dynamic + static shared memory of one CTA
 
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   __shared__ __align__(16) float dsb[NB][CH][G];  // chunks' d_scores, key-major
   __shared__ __align__(16) float red[G * D];      // the CTA's d_q partial of a segment
-  __shared__ int last_s;
+  __shared__ int dpair_s[kDecDefer], dlast_s[kDecDefer];  // deferred segment completions
   __shared__ __align__(8) uint64_t full[NS], empty[NS], ds_full[NB], ds_empty[NB];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -604,9 +617,54 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
   int cur_pair = -1, seg = -1;
   bool ok = true;
 
+  // Completion of the deferred segments: make this CTA's partials visible,
+  // count this CTA in for each of their pairs, and let the last CTA of a pair
+  // sum the partials in CTA order and write d_q.  Deferred to the end of the
+  // chunk loop (or until kDecDefer are pending) because every global round
+  // trip costs microseconds under the streaming load.
+  int ndef = 0;
+  auto complete = [&]() {
+    __threadfence();
+    named_bar_sync(1, P2T);
+    if (t2 == 0) {
+      for (int k = 0; k < ndef; ++k) {
+        const long long fa = (long long)dpair_s[k] * a.cpp;
+        const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+        const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+        dlast_s[k] = ia == ib || atomicAdd(&a.count[dpair_s[k]], 1u) == (unsigned)(ib - ia);
+      }
+    }
+    named_bar_sync(1, P2T);
+    for (int k = 0; k < ndef; ++k) {
+      if (!dlast_s[k]) continue;
+      __threadfence();
+      const int p = dpair_s[k];
+      const long long fa = (long long)p * a.cpp;
+      const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
+      const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
+      const int seq = p / a.n_kv, kv = p % a.n_kv;
+      constexpr int NO = (G * D + P2T - 1) / P2T;  // outputs per thread
+      float t[NO];
+#pragma unroll
+      for (int q = 0; q < NO; ++q) t[q] = 0.f;
+      for (int i = ia; i <= ib; ++i) {
+        const int sg = p - dec_pair0(i, a.n_chunks, a.grid, a.cpp);
+        const float* p2 = a.part2 + ((size_t)i * a.max_seg + sg) * C::SLOT2;
+#pragma unroll
+        for (int q = 0; q < NO; ++q)
+          if (t2 + q * P2T < G * D) t[q] += __ldcg(p2 + t2 + q * P2T);
+      }
+#pragma unroll
+      for (int q = 0; q < NO; ++q)
+        if (t2 + q * P2T < G * D) a.d_q[((size_t)seq * a.n_heads + kv * G) * D + t2 + q * P2T] = t[q];
+    }
+    named_bar_sync(1, P2T);  // dpair_s / dlast_s may be reused
+    ndef = 0;
+  };
+
   // segment `seg` (pair cur_pair) is complete in this CTA: sum the key
-  // groups in shared memory (in key-group order), write the CTA's partial,
-  // and let the last CTA of the pair sum the partials in CTA order
+  // groups in shared memory (in key-group order) and store the CTA's partial;
+  // its completion is deferred
   auto finish = [&]() {
     float x[G][DPT];
     if constexpr (G == 1) {
@@ -638,26 +696,10 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
     float* sl = slots + (size_t)seg * C::SLOT2;
     for (int o = 4 * t2; o < G * D; o += 4 * P2T)
       *reinterpret_cast<float4*>(sl + o) = *reinterpret_cast<const float4*>(red + o);
-    __threadfence();
-    named_bar_sync(1, P2T);  // every partial written; red may be reused
-    const long long fa = (long long)cur_pair * a.cpp;
-    const int ia = dec_cta_of(fa, a.n_chunks, a.grid);
-    const int ib = dec_cta_of(fa + a.cpp - 1, a.n_chunks, a.grid);
-    if (t2 == 0)
-      last_s = ia == ib || atomicAdd(&a.count[cur_pair], 1u) == (unsigned)(ib - ia);
-    named_bar_sync(1, P2T);
-    if (last_s) {  // every CTA of the pair has written its partial: sum in CTA order
-      __threadfence();
-      const int seq = cur_pair / a.n_kv, kv = cur_pair % a.n_kv;
-      for (int o = t2; o < G * D; o += P2T) {
-        float t = 0.f;
-        for (int i = ia; i <= ib; ++i) {
-          const int sg = cur_pair - (int)(dec_begin(i, a.n_chunks, a.grid) / a.cpp);
-          t += __ldcg(a.part2 + ((size_t)i * a.max_seg + sg) * C::SLOT2 + o);
-        }
-        a.d_q[((size_t)seq * a.n_heads + kv * G) * D + o] = t;
-      }
-    }
+    if (t2 == 0) dpair_s[ndef] = cur_pair;
+    ++ndef;
+    named_bar_sync(1, P2T);  // red read out; dpair_s written
+    if (ndef == kDecDefer) complete();
   };
 
   int pair = pair0, lc = lc0;
@@ -722,7 +764,10 @@ __global__ void __launch_bounds__(32 * (1 + DecCfg<D, G>::P2W + DecCfg<D, G>::DS
     }
     if (++lc == a.cpp) lc = 0, ++pair;
   }
-  if (ok && seg >= 0) finish();
+  if (ok && seg >= 0) {
+    finish();
+    complete();
+  }
 }
 
 template <int D, int G>
