@@ -159,8 +159,10 @@ attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
  *   k_hist, v_hist [num_seqs, history_len, n_kv_heads, head_dim]
  *   probs, d_scores [num_seqs, n_heads, history_len]
  *   d_out, d_q      [num_seqs, n_heads, head_dim]
- * head_dim must be a multiple of 4 and <= 256; n_heads % n_kv_heads == 0,
- * n_heads / n_kv_heads <= 16; history_len >= 1.
+ * head_dim is 64, 128 or 256; n_heads % n_kv_heads == 0 and n_heads /
+ * n_kv_heads is 1, 2, 4, 8 or 16; history_len >= 1.  Two kernels on `stream`
+ * (a V pass, then a K pass that may start while the first finishes); the
+ * result does not depend on timing.
  * workspace: >= attn_bwd_decode_workspace_size(p) bytes (256-byte aligned).
  */
 typedef struct {
@@ -192,9 +194,10 @@ attn_status attn_bwd_decode(const attn_bwd_decode_params* p, const float* k_hist
  * Scratch: the partial sums go to one fixed array of
  * ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory inside the
  * library; every GPU that loads the library keeps that array until the
- * process exits.  The array must hold, for at least one history split,
- * num_seqs * n_heads * (1 + 2 * head_dim) floats (e.g. 64 sequences x 8 heads
- * x head_dim 256 take 1 MiB per split); larger problems are rejected with
+ * process exits.  The array must hold the partial sums of at least one
+ * history split, about num_seqs * n_heads * (head_dim + 8) floats plus one
+ * counter per (sequence, KV head) pair (e.g. 64 sequences x 8 heads x
+ * head_dim 256: 0.5 MiB); larger problems are rejected with
  * ATTN_ERR_SCRATCH_LIMIT.  When the usual number of splits does not fit,
  * fewer are used, so results can differ from attn_bwd_decode in the last bits.
  *

@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_entry_point(prob):
 def test_noalloc_rejects_problem_beyond_scratch():
     import torch
     import attention_backward_pass_gb300 as ab
-    # 4096 sequences x 8 heads x (1 + 2*256) floats = 64 MiB for one split > 8 MiB
+    # 4096 sequences x 8 heads x (256 + 8) floats = 34 MiB for one split > 8 MiB
     p = W.DecodeProblem(4096, 8, 1, 256, 16)
     dummy = torch.empty(16, device="cuda")
     with pytest.raises(ab.AttnError) as e:
