@@ -365,6 +365,65 @@ def test_decode_finite_differences():
                 assert abs((fp - fm) / (2 * h) - d_scores[n, hh, j]) < 1e-7
 
 
+def test_decode_kv_finite_differences():
+    """Pass 2 (history gradients) against central differences of the decode
+    loss sum_h d_out_h . out_h w.r.t. k_hist and v_hist, with d_scores from
+    pass 1."""
+    rng = np.random.default_rng(3)
+    N, hist, n_kv, n_heads, D = 2, 5, 2, 4, 3
+    k = rng.standard_normal((N, hist, n_kv, D))
+    v = rng.standard_normal((N, hist, n_kv, D))
+    q = rng.standard_normal((N, n_heads, D))
+    d_out = rng.standard_normal((N, n_heads, D))
+    kv_of = np.arange(n_heads) // (n_heads // n_kv)
+
+    def loss(kk, vv):
+        tot = 0.0
+        for n in range(N):
+            for h in range(n_heads):
+                pr = Dec.softmax_rows(kk[n, :, kv_of[h]] @ q[n, h])
+                tot += d_out[n, h] @ (pr @ vv[n, :, kv_of[h]])
+        return tot
+
+    scores = np.stack([np.stack([k[n, :, kv_of[h]] @ q[n, h] for h in range(n_heads)])
+                       for n in range(N)])
+    probs = Dec.softmax_rows(scores)
+    d_scores, _ = Dec.decode_backward(k, v, probs, d_out)
+    d_k, d_v = Dec.decode_backward_kv(q, probs, d_out, d_scores, n_kv)
+    h = 1e-6
+    fd_k, fd_v = np.zeros_like(k), np.zeros_like(v)
+    for idx in np.ndindex(k.shape):
+        kp, km = k.copy(), k.copy()
+        kp[idx] += h
+        km[idx] -= h
+        fd_k[idx] = (loss(kp, v) - loss(km, v)) / (2 * h)
+        vp, vm = v.copy(), v.copy()
+        vp[idx] += h
+        vm[idx] -= h
+        fd_v[idx] = (loss(k, vp) - loss(k, vm)) / (2 * h)
+    np.testing.assert_allclose(d_k, fd_k, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(d_v, fd_v, rtol=1e-6, atol=1e-8)
+
+
+def test_decode_kv_history_sums():
+    """Summed over the history, d_k vanishes (each head's d_scores sum to 0)
+    and d_v is the sum of the group's d_out (each head's probabilities sum to
+    1)."""
+    rng = np.random.default_rng(4)
+    N, hist, n_kv, n_heads, D = 3, 9, 2, 8, 5
+    k = rng.standard_normal((N, hist, n_kv, D))
+    v = rng.standard_normal((N, hist, n_kv, D))
+    q = rng.standard_normal((N, n_heads, D))
+    d_out = rng.standard_normal((N, n_heads, D))
+    probs = Dec.softmax_rows(rng.standard_normal((N, n_heads, hist)))
+    d_scores, _ = Dec.decode_backward(k, v, probs, d_out)
+    d_k, d_v = Dec.decode_backward_kv(q, probs, d_out, d_scores, n_kv)
+    np.testing.assert_allclose(d_k.sum(axis=1), 0.0, atol=1e-12)
+    G = n_heads // n_kv
+    want = d_out.reshape(N, n_kv, G, D).sum(axis=2)
+    np.testing.assert_allclose(d_v.sum(axis=1), want, rtol=1e-12, atol=1e-12)
+
+
 def test_decode_one_hot_and_delta():
     rng = np.random.default_rng(1)
     N, hist, n_kv, n_heads, D = 1, 8, 1, 3, 5
