@@ -70,6 +70,8 @@ _SIGS = {
                                        _P, _P, ctypes.c_size_t, _P]),
     "attn_bwd_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P,
                                                _P, _P, _P, _P]),
+    "attn_bwd_decode_kv": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P, _P,
+                                          _P, _P, _P]),
     "attn_dropout_keep_mask": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), ctypes.c_int32,
                                               ctypes.c_int32, _P, _P]),
     "attn_bwd_query_range": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), ctypes.c_int32,
@@ -224,6 +226,15 @@ def attn_bwd_decode_noalloc(p, k_hist, v_hist, probs, d_out, d_scores, d_q, stre
                                                 _ptr(v_hist), _ptr(probs), _ptr(d_out),
                                                 _ptr(d_scores), _ptr(d_q), _stream_ptr(stream))
     _check("attn_bwd_decode_noalloc", st)
+
+
+def attn_bwd_decode_kv(p, q, probs, d_out, d_scores, d_k_hist, d_v_hist, stream=None):
+    """Decode backward pass 2 (gradients of k_hist and v_hist) from pass 1's
+    d_scores."""
+    st = load_library().attn_bwd_decode_kv(ctypes.byref(make_decode_params(p)), _ptr(q),
+                                           _ptr(probs), _ptr(d_out), _ptr(d_scores),
+                                           _ptr(d_k_hist), _ptr(d_v_hist), _stream_ptr(stream))
+    _check("attn_bwd_decode_kv", st)
 
 
 def dropout_keep_mask(p, b, h, keep, stream=None):

@@ -399,6 +399,20 @@ static attn_status validate_decode(const attn_bwd_decode_params* p) {
   return ATTN_OK;
 }
 
+attn_status attn_bwd_decode_kv(const attn_bwd_decode_params* p, const float* q,
+                               const float* probs, const float* d_out, const float* d_scores,
+                               float* d_k_hist, float* d_v_hist, void* stream) {
+  attn_status st = validate_decode(p);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[] = {q, probs, d_out, d_scores, d_k_hist, d_v_hist};
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return ATTN_ERR_INVALID;
+  if (launch_decode_kv(*p, q, probs, d_out, d_scores, d_k_hist, d_v_hist,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 size_t attn_bwd_decode_workspace_size(const attn_bwd_decode_params* p) {
   if (validate_decode(p) != ATTN_OK) return 0;
   return align256(decode_partials_floats(*p, decode_num_splits(*p)) * 4);

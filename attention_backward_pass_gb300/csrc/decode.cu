@@ -936,6 +936,153 @@ cudaError_t launch_decode(const attn_bwd_decode_params& p, const float* k_hist,
 
 }  // namespace attnbwd
 
+
+// ------------------------------------------------------------------------
+// Decode backward, pass 2: the history's gradients
+//   d_k_hist[j, kv] = sum_h d_scores_hj q_h,  d_v_hist[j, kv] = sum_h probs_hj d_out_h
+// over the G query heads h of KV head kv (the decode page's pass 2 consumes
+// pass 1's d_scores and takes q; these are the gradients of its forward).
+// Bound by the two history-sized writes.  One CTA per (pair, chunk of 64
+// keys): its threads stage the chunk's d_scores / probs slices [key][head] in
+// shared memory with coalesced loads, hold q and d_out of the group for their
+// DPT head-dim elements in registers, and write each key row with contiguous
+// vector stores.
+// ------------------------------------------------------------------------
+namespace attnbwd {
+namespace {
+
+constexpr int kKvChunk = 64;
+constexpr int kKvThreads = 256;
+
+struct KvArgs {
+  const float* q;
+  const float* probs;
+  const float* d_out;
+  const float* d_scores;
+  float* d_k;
+  float* d_v;
+  int n_heads, n_kv, hist, cpp;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kKvThreads) decode_kv_kernel(const KvArgs a) {
+  constexpr int CH = kKvChunk;
+  constexpr int DPT = G <= 8 ? 4 : 2;  // head-dim elements per thread
+  constexpr int TPK = D / DPT;         // threads per key row
+  constexpr int KGRP = kKvThreads / TPK;
+  static_assert(TPK <= kKvThreads && CH % KGRP == 0, "decode_kv split");
+  __shared__ __align__(16) float ds_s[CH][G];
+  __shared__ __align__(16) float pr_s[CH][G];
+  const int pair = (int)(blockIdx.x / (unsigned)a.cpp), lc = (int)(blockIdx.x % (unsigned)a.cpp);
+  const int seq = pair / a.n_kv, kv = pair % a.n_kv;
+  const int j0 = lc * CH, rows = min(CH, a.hist - j0);
+  const int t = threadIdx.x, kg = t / TPK, d = DPT * (t % TPK);
+  const size_t hrow = (size_t)seq * a.n_heads + kv * G;  // first query head of the group
+  for (int i = t; i < G * CH; i += kKvThreads) {
+    const int g = i / CH, jj = i % CH;
+    float ds = 0.f, pv = 0.f;
+    if (jj < rows) {
+      const size_t gi = (hrow + g) * a.hist + j0 + jj;
+      ds = __ldg(a.d_scores + gi);
+      pv = __ldg(a.probs + gi);
+    }
+    ds_s[jj][g] = ds;
+    pr_s[jj][g] = pv;
+  }
+  // packed (d, d+1) pairs of q and d_out for every head of the group
+  uint64_t q2[G][DPT / 2], o2[G][DPT / 2];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float* qr = a.q + (hrow + g) * D + d;
+    const float* orow = a.d_out + (hrow + g) * D + d;
+    if constexpr (DPT == 4) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(qr));
+      const float4 y = __ldg(reinterpret_cast<const float4*>(orow));
+      q2[g][0] = pk2(x.x, x.y), q2[g][1] = pk2(x.z, x.w);
+      o2[g][0] = pk2(y.x, y.y), o2[g][1] = pk2(y.z, y.w);
+    } else {
+      const float2 x = __ldg(reinterpret_cast<const float2*>(qr));
+      const float2 y = __ldg(reinterpret_cast<const float2*>(orow));
+      q2[g][0] = pk2(x.x, x.y);
+      o2[g][0] = pk2(y.x, y.y);
+    }
+  }
+  __syncthreads();
+  for (int jj = kg; jj < rows; jj += KGRP) {
+    uint64_t dk[DPT / 2], dv[DPT / 2];
+#pragma unroll
+    for (int i = 0; i < DPT / 2; ++i) dk[i] = dv[i] = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float ds = ds_s[jj][g], pv = pr_s[jj][g];
+      const uint64_t ds2 = pk2(ds, ds), pv2 = pk2(pv, pv);
+#pragma unroll
+      for (int i = 0; i < DPT / 2; ++i) {
+        dk[i] = f2fma(ds2, q2[g][i], dk[i]);
+        dv[i] = f2fma(pv2, o2[g][i], dv[i]);
+      }
+    }
+    const size_t row = (((size_t)seq * a.hist + j0 + jj) * a.n_kv + kv) * D + d;
+    if constexpr (DPT == 4) {
+      float x0, x1, x2, x3;
+      up2(dk[0], x0, x1);
+      up2(dk[1], x2, x3);
+      *reinterpret_cast<float4*>(a.d_k + row) = make_float4(x0, x1, x2, x3);
+      up2(dv[0], x0, x1);
+      up2(dv[1], x2, x3);
+      *reinterpret_cast<float4*>(a.d_v + row) = make_float4(x0, x1, x2, x3);
+    } else {
+      float x0, x1;
+      up2(dk[0], x0, x1);
+      *reinterpret_cast<float2*>(a.d_k + row) = make_float2(x0, x1);
+      up2(dv[0], x0, x1);
+      *reinterpret_cast<float2*>(a.d_v + row) = make_float2(x0, x1);
+    }
+  }
+}
+
+template <int D>
+cudaError_t kv_by_group(const KvArgs& a, int G, unsigned grid, cudaStream_t stream) {
+  switch (G) {
+    case 1: decode_kv_kernel<D, 1><<<grid, kKvThreads, 0, stream>>>(a); break;
+    case 2: decode_kv_kernel<D, 2><<<grid, kKvThreads, 0, stream>>>(a); break;
+    case 4: decode_kv_kernel<D, 4><<<grid, kKvThreads, 0, stream>>>(a); break;
+    case 8: decode_kv_kernel<D, 8><<<grid, kKvThreads, 0, stream>>>(a); break;
+    case 16: decode_kv_kernel<D, 16><<<grid, kKvThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_kv(const attn_bwd_decode_params& p, const float* q, const float* probs,
+                             const float* d_out, const float* d_scores, float* d_k, float* d_v,
+                             cudaStream_t stream) {
+  KvArgs a;
+  a.q = q;
+  a.probs = probs;
+  a.d_out = d_out;
+  a.d_scores = d_scores;
+  a.d_k = d_k;
+  a.d_v = d_v;
+  a.n_heads = p.n_heads;
+  a.n_kv = p.n_kv_heads;
+  a.hist = p.history_len;
+  a.cpp = (p.history_len + kKvChunk - 1) / kKvChunk;
+  const long long n = (long long)p.num_seqs * p.n_kv_heads * a.cpp;
+  if (n < 1 || n > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int G = p.n_heads / p.n_kv_heads;
+  switch (p.head_dim) {
+    case 64: return kv_by_group<64>(a, G, (unsigned)n, stream);
+    case 128: return kv_by_group<128>(a, G, (unsigned)n, stream);
+    case 256: return kv_by_group<256>(a, G, (unsigned)n, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attnbwd
+
 // ------------------------------------------------------------------------
 // Decode backward without a caller-supplied workspace.
 //

@@ -109,6 +109,9 @@ cudaError_t launch_decode(const attn_bwd_decode_params& p, const float* k_hist,
                           float* d_scores, float* d_q, float* partials, int n_split,
                           cudaStream_t stream);
 int decode_num_splits(const attn_bwd_decode_params& p);
+cudaError_t launch_decode_kv(const attn_bwd_decode_params& p, const float* q, const float* probs,
+                             const float* d_out, const float* d_scores, float* d_k, float* d_v,
+                             cudaStream_t stream);
 CUresult make_f32_map(CUtensorMap* m, const void* base, int rank, const long long* dims,
                       const int* box, bool swizzle128);
 size_t decode_partials_floats(const attn_bwd_decode_params& p, int n_split);

@@ -133,6 +133,13 @@ def make_decode_inputs(p: DecodeProblem, seed: int):
     return k, v, d_out, logits
 
 
+def make_decode_queries(p: DecodeProblem, seed: int):
+    """q [N,n_heads,D] ~ N(0,1) for the decode pass 2 (its own stream: the
+    pass-1 inputs of the same seed are unchanged)."""
+    g = _rng(seed + 0x51)
+    return g.standard_normal((p.num_seqs, p.n_heads, p.head_dim), dtype=np.float32)
+
+
 # --------------------------------------------------------------------------
 # The five workloads (shapes, masking rules, value distributions).
 # --------------------------------------------------------------------------

@@ -181,6 +181,25 @@ attn_status attn_bwd_decode(const attn_bwd_decode_params* p, const float* k_hist
                             size_t workspace_bytes, void* stream);
 
 /*
+ * Decode backward, pass 2: the gradients of the history.  The decode page's
+ * pass 1 stages d_scores for a pass 2 that also takes the queries q (that
+ * file is not on the pages); read as the gradients of the page's forward
+ * (out_h = sum_j probs_hj v_hist[j, kv], unscaled scores q_h . k_hist[j, kv]):
+ *   d_k_hist[j, kv] = sum_{h of kv} d_scores_hj q_h
+ *   d_v_hist[j, kv] = sum_{h of kv} probs_hj d_out_h
+ *   q, d_out           [num_seqs, n_heads, head_dim]
+ *   probs, d_scores    [num_seqs, n_heads, history_len]   (d_scores from attn_bwd_decode)
+ *   d_k_hist, d_v_hist [num_seqs, history_len, n_kv_heads, head_dim]  (written, every element)
+ * Same parameter rules as attn_bwd_decode; device pointers, 16-byte aligned;
+ * no workspace; one kernel on `stream`.  Errors: ATTN_ERR_INVALID /
+ * ATTN_ERR_UNSUPPORTED for the parameters or pointers, ATTN_ERR_CUDA if the
+ * launch fails.
+ */
+attn_status attn_bwd_decode_kv(const attn_bwd_decode_params* p, const float* q,
+                               const float* probs, const float* d_out, const float* d_scores,
+                               float* d_k_hist, float* d_v_hist, void* stream);
+
+/*
  * attn_bwd_decode for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point.  Some callers cannot give the
  * library a workspace: code that runs where no allocator is available or

@@ -115,6 +115,21 @@ def decode_case(p, seed):
     return dict(k=k, v=v, d_out=d_out, probs=probs)
 
 
+def run_decode_kv_gpu(p, case, q, d_scores, device="cuda"):
+    """Decode pass 2 on the GPU from the given (fp32) d_scores."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    t = {k: torch.from_numpy(np.ascontiguousarray(case[k])).to(device) for k in ("d_out", "probs")}
+    tq = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).to(device)
+    tds = torch.from_numpy(np.ascontiguousarray(d_scores, dtype=np.float32)).to(device)
+    shape = (p.num_seqs, p.history_len, p.n_kv_heads, p.head_dim)
+    d_k = torch.full(shape, float("nan"), device=device)
+    d_v = torch.full(shape, float("nan"), device=device)
+    ab.attn_bwd_decode_kv(p, tq, t["probs"], t["d_out"], tds, d_k, d_v)
+    torch.cuda.synchronize()
+    return d_k.cpu().numpy().astype(np.float64), d_v.cpu().numpy().astype(np.float64)
+
+
 def run_decode_gpu(p, case, device="cuda", repeat=1):
     import torch
     import attention_backward_pass_gb300 as ab

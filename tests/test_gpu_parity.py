@@ -12,7 +12,8 @@ from attention_backward_pass_gb300 import workloads as W
 from oracle import decode as OD
 from oracle import philox
 
-from parity_helpers import TOL, compare, decode_case, make_case, rel_err, run_decode_gpu
+from parity_helpers import (TOL, compare, decode_case, make_case, rel_err, run_decode_gpu,
+                            run_decode_kv_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,6 +140,35 @@ def test_decode_parity(name):
     rds, rdq = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"])
     assert rel_err(ds, rds) <= 2e-3 and rel_err(dq, rdq) <= 2e-3, (rel_err(ds, rds),
                                                                     rel_err(dq, rdq))
+
+
+@pytest.mark.parametrize("name", sorted(DECODE))
+def test_decode_kv_parity(name):
+    """Pass 2 (history gradients) on pass 1's GPU d_scores, against the oracle
+    of both passes in fp64."""
+    p = DECODE[name]
+    case = decode_case(p, seed=7)
+    q = W.make_decode_queries(p, seed=7)
+    ds, _ = run_decode_gpu(p, case)
+    d_k, d_v = run_decode_kv_gpu(p, case, q, ds)
+    rds, _ = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"])
+    rdk, rdv = OD.decode_backward_kv(q, case["probs"], case["d_out"], rds, p.n_kv_heads)
+    assert np.all(np.isfinite(d_k)) and np.all(np.isfinite(d_v))
+    assert rel_err(d_k, rdk) <= 2e-3 and rel_err(d_v, rdv) <= 2e-3, (rel_err(d_k, rdk),
+                                                                    rel_err(d_v, rdv))
+
+
+def test_decode_kv_full_size_sampled():
+    p = W.decode()
+    case = decode_case(p, seed=4)
+    q = W.make_decode_queries(p, seed=4)
+    ds, _ = run_decode_gpu(p, case)
+    d_k, d_v = run_decode_kv_gpu(p, case, q, ds)
+    seqs = [0, 31, 63]
+    rds, _ = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"], seqs=seqs)
+    rdk, rdv = OD.decode_backward_kv(q, case["probs"], case["d_out"], rds, p.n_kv_heads, seqs=seqs)
+    assert np.all(np.isfinite(d_k)) and np.all(np.isfinite(d_v))
+    assert rel_err(d_k[seqs], rdk[seqs]) <= 2e-3 and rel_err(d_v[seqs], rdv[seqs]) <= 2e-3
 
 
 def test_decode_full_size_sampled():
