@@ -43,6 +43,15 @@ def decode_bytes(p) -> int:
     return 4 * (kv + 2 * probs + 2 * dout)
 
 
+def decode_kv_bytes(p) -> int:
+    """Minimum HBM bytes of the decode pass 2: d_k_hist and d_v_hist written,
+    probs and d_scores read, q and d_out read; all fp32."""
+    hist = 2 * p.num_seqs * p.history_len * p.n_kv_heads * p.head_dim
+    rows = 2 * p.num_seqs * p.n_heads * p.history_len
+    vecs = 2 * p.num_seqs * p.n_heads * p.head_dim
+    return 4 * (hist + rows + vecs)
+
+
 def decode_flops(p) -> float:
     """2 flops per multiply-add of d_probs = d_out.v and d_q = sum d_scores k,
     per query head: 4 * history * D per head."""

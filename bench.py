@@ -49,8 +49,11 @@ WORKLOADS = {
                        "masked+dropout B2 H16 Sq512 Sk2048 D64 fp32 causal_offset1536 p0.1"),
     "tiny": (W.tiny, 0, "tiny B1 H2 S64 D64 fp32"),
     "decode": (W.decode, 4, "decode backward: 64 seqs, 8 heads, 1 kv head, D256, history 4096, fp32"),
+    "decode_kv": (W.decode, 4, "decode backward pass 2 (d_k_hist, d_v_hist): 64 seqs, 8 heads, "
+                               "1 kv head, D256, history 4096, fp32"),
 }
 DECODE_METRIC = "decode attention-backward GB/s (d_scores+d_q) and % of HBM peak"
+DECODE_KV_METRIC = "decode attention-backward pass 2 GB/s (d_k_hist+d_v_hist) and % of HBM peak"
 
 
 def parse_args():
@@ -236,10 +239,55 @@ def oracle_sample_tflops(p, numpy_inputs, O_np, LSE_np, budget_s: float, rng_see
 
 # --------------------------------------------------------------- main arms
 
+def run_reference_decode(args):
+    """Reference arm for the decode workloads: the oracle on one sequence per
+    step (fp64 numpy on the host cores), value in the arm's GB/s unit."""
+    make, seed, desc = WORKLOADS[args.workload]
+    p = make()
+    kv_pass = args.workload == "decode_kv"
+    from oracle import decode as OD
+    k, v, d_out, logits = W.make_decode_inputs(p, seed)
+    e = np.exp(logits - logits.max(axis=-1, keepdims=True))  # input synthesis
+    probs = e / e.sum(axis=-1, keepdims=True)
+    nbytes = MET.decode_kv_bytes(p) if kv_pass else MET.decode_bytes(p)
+    per_seq = nbytes / p.num_seqs
+    if kv_pass:
+        q = W.make_decode_queries(p, seed)
+        d_scores, _ = OD.decode_backward(k, v, probs, d_out)  # untimed inputs
+    vals = []
+    for step in range(args.warmup + args.steps):
+        n = step % p.num_seqs
+        t0 = time.perf_counter()
+        if kv_pass:
+            OD.decode_backward_kv(q, probs, d_out, d_scores, p.n_kv_heads, seqs=[n])
+        else:
+            OD.decode_backward(k, v, probs, d_out, seqs=[n])
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            vals.append(per_seq / dt / 1e9)
+    value = statistics.mean(vals)
+    sample = f"one sequence of {p.num_seqs} per step, fp64 numpy"
+    line = {
+        "impl": "reference", "metric": DECODE_KV_METRIC if kv_pass else DECODE_METRIC,
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": nbytes / (value * 1e9) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": desc, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload in ("decode", "decode_kv"):
+        return run_reference_decode(args)
     make, seed, desc = WORKLOADS[args.workload]
     p = make()
     from oracle import attention as OA
@@ -453,7 +501,8 @@ def run_decode(args):
         dist.init_process_group(backend="nccl")
     device = torch.device("cuda", torch.cuda.current_device())
     ab.load_library()
-    make, seed, desc = WORKLOADS["decode"]
+    kv_pass = args.workload == "decode_kv"
+    make, seed, desc = WORKLOADS[args.workload]
     p = make()
     k, v, d_out, logits = W.make_decode_inputs(p, seed)
     lg = torch.from_numpy(logits).to(device)
@@ -466,6 +515,18 @@ def run_decode(args):
 
     def step():
         ab.attn_bwd_decode(p, t["k"], t["v"], probs, t["d_out"], d_scores, d_q, ws)
+
+    if kv_pass:
+        # pass 2 consumes pass 1's d_scores (computed once, before timing)
+        step()
+        q_np = W.make_decode_queries(p, seed)
+        q_t = torch.from_numpy(q_np).to(device)
+        hshape = (p.num_seqs, p.history_len, p.n_kv_heads, p.head_dim)
+        d_k = torch.empty(hshape, device=device)
+        d_v = torch.empty(hshape, device=device)
+
+        def step():
+            ab.attn_bwd_decode_kv(p, q_t, probs, t["d_out"], d_scores, d_k, d_v)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -491,7 +552,7 @@ def run_decode(args):
         tt = torch.tensor([total], device=device)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         total = float(tt.item())
-    nbytes = MET.decode_bytes(p)
+    nbytes = MET.decode_kv_bytes(p) if kv_pass else MET.decode_bytes(p)
     value = nbytes * world * args.steps / (total * 1e-3) / 1e9
     peaks, src = load_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -499,10 +560,14 @@ def run_decode(args):
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import decode as OD2
         pr = probs.cpu().numpy()
+        ds_np = d_scores.cpu().numpy() if kv_pass else None
         t0 = time.perf_counter()
         n = 0
         while time.perf_counter() - t0 < 10.0 and n < p.num_seqs:
-            OD2.decode_backward(k, v, pr, d_out, seqs=[n])
+            if kv_pass:
+                OD2.decode_backward_kv(q_np, pr, d_out, ds_np, p.n_kv_heads, seqs=[n])
+            else:
+                OD2.decode_backward(k, v, pr, d_out, seqs=[n])
             n += 1
         secs = time.perf_counter() - t0
         cpu = {"value": nbytes / p.num_seqs * n / secs / 1e9, "unit": "GB/s",
@@ -511,7 +576,8 @@ def run_decode(args):
     if rank == 0:
         mean_ms = statistics.mean(ms)
         line = {
-            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "metric": DECODE_KV_METRIC if kv_pass else DECODE_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -520,10 +586,12 @@ def run_decode(args):
             "roofline": {"bound": "hbm", "achieved": nbytes / (mean_ms * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s",
                          "frac": nbytes / (mean_ms * 1e-3) / 1e9 / peak,
-                         "traffic": read_traffic("passes", prefix="decode_"),
-                         "kernel": "decode_dp_kernel + decode_dq_kernel",
+                         "traffic": read_traffic("kv" if kv_pass else "passes", prefix="decode_"),
+                         "kernel": "decode_kv_kernel" if kv_pass
+                         else "decode_dp_kernel + decode_dq_kernel",
                          "peak_source": f"{src} hbm_gbs"},
-            "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": None,
+            "gpu_launches": (1 if kv_pass else 2) * args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -535,7 +603,7 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload == "decode":
+    if args.workload in ("decode", "decode_kv"):
         return run_decode(args)
     return run_ours(args)
 
