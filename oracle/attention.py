@@ -142,6 +142,32 @@ def delta(dO_rows: np.ndarray, O_rows: np.ndarray) -> np.ndarray:
     return np.sum(np.asarray(dO_rows, np.float64) * np.asarray(O_rows, np.float64), axis=-1)
 
 
+def row_lse(s: np.ndarray, hard: np.ndarray) -> np.ndarray:
+    """LSE_i = log sum over non-hard j of exp(s_ij), shifted by the row
+    maximum; 3e38 for a row with no non-hard key (page 2, flash_bwd_dq sweep 1:
+    lse = m + log l, "fully masked row")."""
+    sm = np.where(hard, -np.inf, s)
+    m = np.max(sm, axis=1, initial=-np.inf)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.where(hard, 0.0, np.exp(np.where(hard, 0.0, s - m_safe[:, None])))
+    l = e.sum(axis=1)
+    return np.where(empty, EMPTY_ROW_LSE, m_safe + np.log(np.where(empty, 1.0, l)))
+
+
+def lse(p, Q, K, mask=None, groups=None):
+    """Row log-sum-exp of the scores for callers without a saved LSE (page 2,
+    flash_bwd_dq sweep 1), fp64 [B, H, Sq]; only the requested (b, kv-head)
+    groups are filled (all by default).  Dropout does not enter."""
+    LSE = np.zeros(p.lse_shape(), dtype=np.float64)
+    G = p.num_heads // p.num_kv_heads
+    for b, kvh in _groups(p, groups):
+        for h in range(kvh * G, (kvh + 1) * G):
+            s, hard = scores(p, Q, K, mask, b, h)
+            LSE[b, h] = row_lse(s, hard)
+    return LSE
+
+
 def forward(p, Q, K, V, mask=None, groups=None):
     """O and LSE consistent with the backward's conventions (used only to
     synthesise backward inputs).  LSE_i = log sum over non-hard j of
@@ -156,18 +182,13 @@ def forward(p, Q, K, V, mask=None, groups=None):
         v = _kv_slice(p, V, b, kvh).astype(np.float64)
         for h in range(kvh * G, (kvh + 1) * G):
             s, hard = scores(p, Q, K, mask, b, h)
-            sm = np.where(hard, -np.inf, s)
-            m = np.max(sm, axis=1, initial=-np.inf)
-            empty = ~np.isfinite(m)
-            m_safe = np.where(empty, 0.0, m)
-            e = np.where(hard, 0.0, np.exp(np.where(hard, 0.0, s - m_safe[:, None])))
-            l = e.sum(axis=1)
-            lse = np.where(empty, EMPTY_ROW_LSE, m_safe + np.log(np.where(empty, 1.0, l)))
-            P = np.where(hard, 0.0, np.exp(np.where(hard, 0.0, s - lse[:, None])))
+            lse_row = row_lse(s, hard)
+            empty = lse_row == EMPTY_ROW_LSE
+            P = np.where(hard, 0.0, np.exp(np.where(hard, 0.0, s - lse_row[:, None])))
             P[empty] = 0.0
             Mdrop = multiplier(p, b, h)
             _set_q(p, O, b, h, (P * Mdrop) @ v)
-            LSE[b, h] = lse
+            LSE[b, h] = lse_row
     return O, LSE
 
 

@@ -220,6 +220,51 @@ def test_fully_masked_rows():
     assert np.all(np.isfinite(dK)) and np.all(np.isfinite(dV))
 
 
+@pytest.mark.parametrize("name", ["plain", "causal", "causal_window_offset", "mask",
+                                  "gqa_bshd", "everything"])
+def test_lse_against_torch_logsumexp(name):
+    # the LSE sweep alone (no forward): torch's logsumexp over the allowed
+    # scores; rows with no allowed key are -inf there and 3e38 in the oracle
+    p = small(**VARIANTS[name])
+    Q, K, V, dO, mask = inputs64(p, seed=21)
+    _, lse_t, _, _, _ = _torch_reference(p, Q, K, V, dO, mask)
+    got = A.lse(p, Q, K, mask)
+    empty = ~np.isfinite(lse_t)
+    np.testing.assert_allclose(got[~empty], lse_t[~empty], rtol=1e-12, atol=1e-12)
+    assert np.all(got[empty] == A.EMPTY_ROW_LSE)
+
+
+def test_lse_online_recurrence_and_dropout_independence():
+    # the page's sweep 1 taken key by key (running maximum m, running sum l
+    # rescaled by exp(m - m_new)) in plain Python on a tiny case, with rows
+    # that have no visible key; dropout does not change the LSE
+    p = small(causal=1, causal_offset=1, window=2, has_mask=1, seq_q=6, seq_k=5)
+    Q, K, V, dO, mask = inputs64(p, seed=4, mask_frac=0.4)
+    # finite additive values where the mask is not hard
+    mask = np.where(mask <= -1e30, mask, np.random.default_rng(3).normal(size=mask.shape))
+    got = A.lse(p, Q, K, mask)
+    G = p.num_heads // p.num_kv_heads
+    for h in range(p.num_heads):
+        for i in range(p.seq_q):
+            m, l = -math.inf, 0.0
+            for j in range(p.seq_k):
+                qa = i + p.causal_offset
+                if j > qa or abs(qa - j) >= p.window:
+                    continue
+                mv = mask[0, 0, i, j]
+                if mv <= -1e30:
+                    continue
+                s = p.scale * sum(Q[0, h, i, d] * K[0, h // G, j, d] for d in range(4)) + mv
+                m_new = max(m, s)
+                l = l * math.exp(m - m_new) + math.exp(s - m_new)
+                m = m_new
+            want = m + math.log(l) if l > 0 else A.EMPTY_ROW_LSE
+            assert abs(got[0, h, i] - want) <= 1e-12 * max(1.0, abs(want)), (h, i)
+    pd = small(causal=1, causal_offset=1, window=2, has_mask=1, seq_q=6, seq_k=5,
+               dropout_prob=0.5, seed=7)
+    np.testing.assert_array_equal(A.lse(pd, Q, K, mask), got)
+
+
 def _golden(name):
     vals = {}
     with open(os.path.join(GOLDEN, name)) as f:
