@@ -65,6 +65,7 @@ _SIGS = {
                                       _P, _P, ctypes.c_size_t, _P]),
     "attn_bwd_finish": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, ctypes.c_size_t,
                                        _P]),
+    "attn_bwd_lse": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P]),
     "attn_bwd_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdDecodeParams)]),
     "attn_bwd_decode": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P, _P, _P,
                                        _P, _P, ctypes.c_size_t, _P]),
@@ -149,7 +150,8 @@ def alloc_workspace(p, device="cuda"):
 
 
 def attn_bwd(p, Q, K, V, O, dO, LSE, mask, dQ, dK, dV, workspace, stream=None):
-    """Enqueue the backward pass; outputs dQ, dK, dV are overwritten."""
+    """Enqueue the backward pass; outputs dQ, dK, dV are overwritten.
+    LSE=None recomputes the row log-sum-exp first (into the workspace)."""
     lib = load_library()
     prm = make_params(p)
     st = lib.attn_bwd(ctypes.byref(prm), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
@@ -186,10 +188,18 @@ def attn_bwd_finish(p, dQ, workspace, stream=None):
     _check("attn_bwd_finish", st)
 
 
-def kernels_per_call(p) -> int:
-    """Kernels one attn_bwd call launches (prepare, tile kernel, and for bf16
-    the dQ conversion)."""
-    return 1 + 1 + (1 if p.dtype == ATTN_BF16 else 0)
+def attn_bwd_lse(p, Q, K, mask, LSE, stream=None):
+    """Row log-sum-exp of the scores into LSE [B, H, Sq] (fp32, 3e38 for
+    rows without a visible, non-hard key)."""
+    st = load_library().attn_bwd_lse(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(mask),
+                                     _ptr(LSE), _stream_ptr(stream))
+    _check("attn_bwd_lse", st)
+
+
+def kernels_per_call(p, recompute_lse: bool = False) -> int:
+    """Kernels one attn_bwd call launches (the LSE sweep when no LSE is
+    given, prepare, tile kernel, and for bf16 the dQ conversion)."""
+    return (1 if recompute_lse else 0) + 1 + 1 + (1 if p.dtype == ATTN_BF16 else 0)
 
 
 def make_decode_params(p) -> AttnBwdDecodeParams:

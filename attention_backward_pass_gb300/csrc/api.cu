@@ -263,13 +263,56 @@ bool all_aligned(std::initializer_list<const void*> ptrs) {
 
 }  // namespace
 
-attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
-                             const void* O, const void* dO, const float* LSE, void* dQ,
-                             void* workspace, size_t workspace_bytes, void* stream_v) {
+namespace {
+
+// Row log-sum-exp on the tensor cores, written either as LSE [B,H,Sq]
+// (out_mode 0) or as -LSE*log2(e) into the workspace rows the tile kernel
+// reads (out_mode 1, sq_pad rows per (b, h)).
+attn_status run_lse(const attn_bwd_params* p, const void* Q, const void* K, const float* mask,
+                    float* out, int out_mode, int sq_pad, cudaStream_t stream) {
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk;
+  if (make_map(&tq, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
+               128) != CUDA_SUCCESS ||
+      make_map(&tk, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
+               lse_block_n(p->dtype, p->head_dim)) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  LseArgs a;
+  memset(&a, 0, sizeof(a));
+  a.B = p->batch;
+  a.H = p->num_heads;
+  a.group = p->num_heads / p->num_kv_heads;
+  a.Sq = p->seq_q;
+  a.Sk = p->seq_k;
+  a.sq_pad = sq_pad;
+  a.scale_log2e = p->scale * kLog2e;
+  a.causal = p->causal;
+  a.causal_offset = p->causal_offset;
+  a.window = p->window;
+  a.has_mask = p->has_mask;
+  a.msb = p->mask_stride_b;
+  a.msh = p->mask_stride_h;
+  a.msq = p->mask_stride_q;
+  a.msk = p->mask_stride_k;
+  a.mask = mask;
+  a.mask_vec = p->has_mask && aligned16(mask) && a.msk == 1 && a.msq % 4 == 0 &&
+               a.msh % 4 == 0 && a.msb % 4 == 0;
+  a.out_mode = out_mode;
+  a.out = out;
+  a.err = err;
+  return launch_lse(*p, tq, tk, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// attn_bwd_prepare without the LSE check: LSE == NULL leaves the workspace's
+// -LSE*log2(e) rows as run_lse wrote them.
+attn_status prepare_impl(const attn_bwd_params* p, const void* Q, const void* K, const void* O,
+                         const void* dO, const float* LSE, void* dQ, void* workspace,
+                         size_t workspace_bytes, void* stream_v) {
   Plan pl;
   attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
   if (st != ATTN_OK) return st;
-  if (!all_aligned({Q, K, O, dO, LSE})) return ATTN_ERR_INVALID;
+  if (!all_aligned({Q, K, O, dO})) return ATTN_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   cudaError_t e;
   if (p->dtype == ATTN_BF16) {
@@ -281,6 +324,26 @@ attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void
                         stream);
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
+                             const void* O, const void* dO, const float* LSE, void* dQ,
+                             void* workspace, size_t workspace_bytes, void* stream_v) {
+  const attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!LSE || !aligned16(LSE)) return ATTN_ERR_INVALID;
+  return prepare_impl(p, Q, K, O, dO, LSE, dQ, workspace, workspace_bytes, stream_v);
+}
+
+attn_status attn_bwd_lse(const attn_bwd_params* p, const void* Q, const void* K,
+                         const float* mask, float* LSE, void* stream) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!all_aligned({Q, K, LSE})) return ATTN_ERR_INVALID;
+  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
+  return run_lse(p, Q, K, mask, LSE, 0, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
@@ -375,9 +438,18 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
                      void* stream) {
   attn_status st = validate(p);
   if (st != ATTN_OK) return st;
-  if (!all_aligned({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID;
+  if (!all_aligned({Q, K, V, O, dO, dQ, dK, dV})) return ATTN_ERR_INVALID;
+  if (LSE && !aligned16(LSE)) return ATTN_ERR_INVALID;
   if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
-  st = attn_bwd_prepare(p, Q, K, O, dO, LSE, dQ, workspace, workspace_bytes, stream);
+  if (!LSE) {
+    // no saved LSE: recompute it into the workspace rows the tiles read
+    Plan pl;
+    st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
+    if (st != ATTN_OK) return st;
+    st = run_lse(p, Q, K, mask, pl.lse2, 1, pl.wl.sq_pad, reinterpret_cast<cudaStream_t>(stream));
+    if (st != ATTN_OK) return st;
+  }
+  st = prepare_impl(p, Q, K, O, dO, LSE, dQ, workspace, workspace_bytes, stream);
   if (st != ATTN_OK) return st;
   st = attn_bwd_tiles(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, workspace_bytes, stream);
   if (st != ATTN_OK) return st;

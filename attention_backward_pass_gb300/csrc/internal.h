@@ -116,4 +116,25 @@ CUresult make_f32_map(CUtensorMap* m, const void* base, int rank, const long lon
                       const int* box, bool swizzle128);
 size_t decode_partials_floats(const attn_bwd_decode_params& p, int n_split);
 
+// Row log-sum-exp (the WGSL page's sweep 1) on the tensor cores.
+struct LseArgs {
+  int B, H, group, Sq, Sk, sq_pad;
+  float scale_log2e;  // scale * log2(e)
+  int causal;
+  long long causal_offset, window;
+  int has_mask, mask_vec;  // mask_vec: rows are contiguous and 16-byte aligned
+  long long msb, msh, msq, msk;
+  const float* mask;
+  int out_mode;  // 0: LSE [B*H][Sq] (3e38 for empty rows); 1: -LSE*log2(e) [B*H][sq_pad], -inf
+  float* out;
+  unsigned int* err;
+};
+constexpr float kHardMask = -1.0e30f;     // a mask value at or below this hides the pair
+constexpr float kEmptyRowLse = 3.0e38f;   // LSE of a row with no probability mass
+// tq: Q in the problem's layout, boxes of 128 rows; tk: K, boxes of
+// lse_block_n(dtype, head_dim) rows.
+int lse_block_n(int dtype, int head_dim);
+cudaError_t launch_lse(const attn_bwd_params& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const LseArgs& a, cudaStream_t stream);
+
 }  // namespace attnbwd

@@ -77,10 +77,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const void* __restrict__ O,
     const long long w = (long long)bh * sq_pad + i;
     if (i < Sq) {
       delta[w] = acc;
-      lse2[w] = -LSE[(long long)bh * Sq + i] * kLog2e;
+      if (LSE) lse2[w] = -LSE[(long long)bh * Sq + i] * kLog2e;
     } else {
       delta[w] = 0.f;
-      lse2[w] = __int_as_float(0xff800000);  // -inf: P = exp2(x - inf) = 0
+      if (LSE) lse2[w] = __int_as_float(0xff800000);  // -inf: P = exp2(x - inf) = 0
     }
   }
 }
@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(256) prep_f32_kernel(
       if (c == 0) {
         const long long w = (long long)bh * sq_pad + s;
         delta[w] = s < S ? acc : 0.f;
-        nlse[w] = s < S ? -LSE[(long long)bh * Sq + s] * kLog2e : __int_as_float(0xff800000);
+        if (LSE)
+          nlse[w] = s < S ? -LSE[(long long)bh * Sq + s] * kLog2e : __int_as_float(0xff800000);
       }
     }
   }

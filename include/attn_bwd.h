@@ -108,6 +108,8 @@ size_t attn_bwd_workspace_size(const attn_bwd_params* p);
  *   LSE: fp32 [B, H, Sq], natural-log log-sum-exp of each row's scores from the
  *        forward pass; a row with no probability mass may hold any value
  *        (the WGSL page stores 3e38) -- its gradients come out as 0.
+ *        NULL: the pass recomputes it first (attn_bwd_lse, written into the
+ *        workspace), as the WGSL page's flash_bwd_dq does in its sweep 1.
  *   mask: fp32 additive mask addressed with p->mask_stride_*; NULL iff !has_mask.
  *   dQ (query-side), dK, dV (key-side): outputs, overwritten.  Keys that no
  *        query sees get dK = dV = 0.
@@ -141,11 +143,29 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
 attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
                              const void* O, const void* dO, const float* LSE, void* dQ,
                              void* workspace, size_t workspace_bytes, void* stream);
+/* (attn_bwd_prepare needs a non-NULL LSE; only attn_bwd recomputes it.) */
 attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
                            const void* dO, const float* mask, void* dQ, void* dK, void* dV,
                            void* workspace, size_t workspace_bytes, void* stream);
 attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/*
+ * Row log-sum-exp of the scores (WGSL page "flash_attention_v2_backward.wgsl",
+ * flash_bwd_dq, sweep 1), for callers that did not keep the forward's LSE:
+ *   LSE_i = log sum_j exp(s_ij)  over the visible keys j with mask_ij > -1e30,
+ *   s_ij  = scale * Q_i . K_j + mask_ij,
+ * and 3e38 for a row with no such key.  Dropout does not enter (the forward's
+ * softmax normaliser is taken before dropout).
+ *   Q, K: as for attn_bwd (p->layout, p->dtype); fp32 inputs are multiplied
+ *        as TF32, the precision of the backward's own score product.
+ *   mask: as for attn_bwd; NULL iff !has_mask.
+ *   LSE:  fp32 [B, H, Sq], written (every row).
+ * Device pointers, 16-byte aligned; one kernel on `stream`, no workspace.
+ * Errors: ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED (head_dim), ATTN_ERR_CUDA.
+ */
+attn_status attn_bwd_lse(const attn_bwd_params* p, const void* Q, const void* K,
+                         const float* mask, float* LSE, void* stream);
 
 /*
  * Decode (one query per head) backward, pass 1 of the decode page

@@ -57,12 +57,13 @@ def make_case(p, seed, groups=None, fill_lse=1.0e4):
     return dict(Q=Q, K=K, V=V, dO=dO, mask=mask, O=O, LSE=LSE)
 
 
-def run_gpu(p, case, device="cuda", repeat=1):
-    """Runs attn_bwd through the C ABI; returns fp64 numpy dQ, dK, dV."""
+def run_gpu(p, case, device="cuda", repeat=1, recompute_lse=False):
+    """Runs attn_bwd through the C ABI; returns fp64 numpy dQ, dK, dV.
+    recompute_lse: pass no LSE, so the pass computes it itself."""
     import torch
     import attention_backward_pass_gb300 as ab
     t = {k: _torch_io(case[k], p.dtype, device) for k in ("Q", "K", "V", "O", "dO")}
-    lse = torch.from_numpy(case["LSE"]).to(device)
+    lse = None if recompute_lse else torch.from_numpy(case["LSE"]).to(device)
     mask = torch.from_numpy(case["mask"]).to(device) if case["mask"] is not None else None
     tdt = torch.bfloat16 if p.dtype == W.DTYPE_BF16 else torch.float32
     dQ = torch.full(p.q_shape(), float("nan"), dtype=tdt, device=device)
@@ -94,9 +95,9 @@ def select_groups(p, arr, groups, side):
     return np.stack(out)
 
 
-def compare(p, case, groups=None, repeat=1):
+def compare(p, case, groups=None, repeat=1, recompute_lse=False):
     """Returns {name: rel_err} for dQ, dK, dV (on the sampled groups if given)."""
-    gpu = run_gpu(p, case, repeat=repeat)
+    gpu = run_gpu(p, case, repeat=repeat, recompute_lse=recompute_lse)
     ref = oracle_grads(p, case, groups)
     errs = {}
     for name, g, r, side in zip(("dQ", "dK", "dV"), gpu, ref, ("q", "k", "k")):
@@ -107,6 +108,51 @@ def compare(p, case, groups=None, repeat=1):
             errs[name] = rel_err(select_groups(p, g, groups, side),
                                  select_groups(p, r, groups, side))
     return errs
+
+
+def lse_bound(p, Q, K, mask, ref):
+    """Per-row bound on |LSE_gpu - LSE_oracle| derived from the arithmetic.
+    The LSE is a smooth maximum of the row's scores (its gradient is a
+    probability vector), so its error is at most the largest score error plus
+    the error of the reduction:
+      score:  (2 u_in + D 2^-23) |scale| max_j sum_d |q_id k_jd|, u_in = 2^-10 for
+              fp32 inputs read as TF32 (truncation or rounding), 0 for bf16
+              inputs (exact products), fp32 accumulation over D terms;
+      reduce: Sk 2^-24 (recursive fp32 sum of at most Sk terms) + 2^-20 (ex2 /
+              log2 approximations) + 2^-22 (|LSE| + max|mask|) (rounding of the
+              scaled scores and of the result).
+    Returns an array shaped like ``ref`` ([B, H, Sq])."""
+    G = p.num_heads // p.num_kv_heads
+    u_in = 2.0 ** -10 if p.dtype == W.DTYPE_F32 else 0.0
+    mmax = 0.0
+    if mask is not None:
+        mv = np.asarray(mask, dtype=np.float64)
+        mv = mv[mv > -1e30]
+        mmax = float(np.max(np.abs(mv))) if mv.size else 0.0
+    out = np.zeros_like(ref)
+    for b in range(p.batch):
+        for h in range(p.num_heads):
+            q = np.abs(Q[b, h] if p.layout == W.LAYOUT_BHSD else Q[b, :, h]).astype(np.float64)
+            kk = K[b, h // G] if p.layout == W.LAYOUT_BHSD else K[b, :, h // G]
+            a = (q @ np.abs(kk).astype(np.float64).T).max(axis=1)
+            out[b, h] = ((2 * u_in + p.head_dim * 2.0 ** -23) * abs(p.scale) * a
+                         + p.seq_k * 2.0 ** -24 + 2.0 ** -20
+                         + 2.0 ** -22 * (np.abs(ref[b, h]) + mmax))
+    return out
+
+
+def run_lse_gpu(p, Q, K, mask, device="cuda"):
+    """attn_bwd_lse through the C ABI; returns fp64 numpy LSE [B, H, Sq]."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    q = _torch_io(Q, p.dtype, device)
+    k = _torch_io(K, p.dtype, device)
+    m = torch.from_numpy(mask).to(device) if mask is not None else None
+    out = torch.full((p.batch, p.num_heads, p.seq_q), float("nan"), device=device)
+    ab.attn_bwd_lse(p, q, k, m, out)
+    torch.cuda.synchronize()
+    assert ab.check_device_error() == 0
+    return out.cpu().numpy().astype(np.float64)
 
 
 def decode_case(p, seed):

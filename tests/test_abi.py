@@ -74,9 +74,17 @@ def test_null_pointers_and_mask_mismatch(lib):
     # has_mask = 0 but a mask pointer given
     args_mask = [fake] * 7 + [fake] * 3
     assert lib.attn_bwd(ctypes.byref(prm), *args_mask, fake, 1 << 30, None) == -1
-    # a null tensor
-    args_null = [fake] * 5 + [None] + [None] + [fake] * 3
+    # a null tensor (O; a null LSE is legal and means "recompute it")
+    args_null = [fake] * 3 + [None] + [fake] + [fake] + [None] + [fake] * 3
     assert lib.attn_bwd(ctypes.byref(prm), *args_null, fake, 1 << 30, None) == -1
+    # the LSE sweep: null Q or output, mask pointer without has_mask, misaligned
+    assert lib.attn_bwd_lse(ctypes.byref(prm), None, fake, None, fake, None) == -1
+    assert lib.attn_bwd_lse(ctypes.byref(prm), fake, fake, None, None, None) == -1
+    assert lib.attn_bwd_lse(ctypes.byref(prm), fake, fake, fake, fake, None) == -1
+    assert lib.attn_bwd_lse(ctypes.byref(prm), fake, ctypes.c_void_p(4100), None, fake, None) == -1
+    # attn_bwd_prepare needs the LSE
+    assert lib.attn_bwd_prepare(ctypes.byref(prm), fake, fake, fake, fake, None, fake, fake,
+                                1 << 30, None) == -1
     # misaligned pointer
     args_mis = [ctypes.c_void_p(4100)] + [fake] * 5 + [None] + [fake] * 3
     assert lib.attn_bwd(ctypes.byref(prm), *args_mis, fake, 1 << 30, None) == -1
