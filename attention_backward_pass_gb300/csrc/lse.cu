@@ -6,9 +6,9 @@
 // Persistent: one CTA per SM walks work items (a tile of 128 query rows of
 // one (batch, query head)), largest first.  The scores come from the tensor
 // cores, S [128 queries, BN keys] = Q . K^T per key tile, so TMEM lane r holds
-// query row r and every reduction thread owns one row and a quarter of the
-// key columns: maximum and sum stay in registers, and the four quarters of a
-// row are merged through shared memory once per item.  The pipeline runs on
+// query row r and every reduction thread owns one row and a share of the
+// key columns: maximum and sum stay in registers, and the four partial sums of
+// a row are merged through shared memory once per item.  The pipeline runs on
 // across items: Q tiles are double-buffered, K tiles stream through a ring,
 // scores through NSB TMEM buffers.
 //
@@ -18,7 +18,9 @@
 //   warp 2      TMEM allocator
 //   warp 3      idle
 //   warps 4-19  reduction: warp w reads TMEM sub-partition w % 4 (its 32
-//               query rows) and quarter (w - 4) / 4 of the key columns
+//               query rows); without a mask two groups of 8 warps take
+//               alternate key tiles, half of the columns each, with a mask
+//               every warp takes a quarter of every tile's columns
 // Scores are kept in the log2 domain, x = s * scale * log2(e) + mask * log2(e),
 // so every exponential is one ex2; the row result is LSE = ln 2 * (m + log2 l).
 // fp32 inputs are fetched as TF32 (the operand type of the products), exactly
@@ -52,10 +54,11 @@ struct LseLayout {
   static constexpr int NQ = 2;           // Q buffers
   static constexpr int NK = (200 * 1024 - NQ * Q_BYTES) / K_BYTES >= 4 ? 4 : 2;  // K stages
   static constexpr int NSB = 512 / BN >= 4 ? 4 : 512 / BN;  // score buffers in TMEM
-  static constexpr int QC = BN / 4;      // key columns per reduction thread
+  static constexpr int QC = BN / 4;      // key columns per reduction thread (with a mask)
+  static constexpr int QC2 = BN / 2;     // key columns per reduction thread (without)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
-  static constexpr int OFF_RED = OFF_K + NK * K_BYTES;  // [4][BM] (m, l) per quarter
+  static constexpr int OFF_RED = OFF_K + NK * K_BYTES;  // [4][BM] partial (m, l)
   static constexpr int OFF_BAR = OFF_RED + 4 * BM * 8;
   static constexpr int NUM_BARS = 2 * NQ + 2 * NK + 2 * NSB + 1;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
@@ -66,6 +69,7 @@ struct LseLayout {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(NSB * BN <= 512 && NK >= 2, "buffers");
   static_assert(D % W == 0 && QC % 16 == 0, "whole column blocks and TMEM loads");
+  static_assert(NSB % 2 == 0, "the two reduction groups take alternate buffers");
 };
 
 // Bounded wait that ignores the error word: used only on the unwinding path to
@@ -145,6 +149,46 @@ __device__ __forceinline__ float tree_ext(const float (&v)[QC]) {
   return t8[0];
 }
 
+// One thread's share of a tile: N consecutive keys from kb of one row, whose
+// visible keys are [lo, hi).  Updates the running maximum m and sum l (log2
+// domain).  A share with no visible key is skipped; one that is wholly visible
+// and unmasked needs only the scores (max of s * c is c * max s, or c * min s
+// for a negative scale); otherwise every key is tested.
+template <int N, bool MASK, typename MV>
+__device__ __forceinline__ void lse_share(const uint32_t (&sv)[N], const MV (&mv)[N], int kb,
+                                          int lo, int hi, float c, uint64_t c2, uint64_t one2,
+                                          float& m, float& l) {
+  if (kb >= hi || kb + N <= lo) return;
+  if (!MASK && kb >= lo && kb + N <= hi) {
+    float sf[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) sf[e] = __uint_as_float(sv[e]);
+    const float mx = c >= 0.f ? tree_ext<N, true>(sf) * c : tree_ext<N, false>(sf) * c;
+    const float mn = fmaxf(m, mx);
+    const float sum = sum_ex2<N>(sf, c2, lse_pk2(-mn, -mn));
+    l = fmaf(l, lse_ex2(m - mn), sum);
+    m = mn;
+  } else {
+    float x[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      bool vis = (unsigned)(kb + e - lo) < (unsigned)(hi - lo);
+      float add = 0.f;
+      if constexpr (MASK) {
+        vis = vis && mv[e] > kHardMask;
+        add = mv[e] * kLog2e;
+      }
+      x[e] = vis ? fmaf(__uint_as_float(sv[e]), c, add) : -INFINITY;
+    }
+    const float mn = fmaxf(m, tree_ext<N, true>(x));
+    if (mn != -INFINITY) {
+      const float sum = sum_ex2<N>(x, one2, lse_pk2(-mn, -mn));
+      l = fmaf(l, lse_ex2(m - mn), sum);
+      m = mn;
+    }
+  }
+}
+
 __device__ __forceinline__ void red_sync() {
   asm volatile("bar.sync 1, 512;" ::: "memory");
 }
@@ -198,7 +242,7 @@ __global__ void __launch_bounds__(kLseThreads, 1)
                const LseArgs a) {
   using L = LseLayout<BF16, D>;
   constexpr int BM = L::BM, BN = L::BN, NK = L::NK, NSB = L::NSB, NQ = L::NQ, W = L::W,
-                QC = L::QC;
+                QC = L::QC, QC2 = L::QC2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -229,7 +273,9 @@ __global__ void __launch_bounds__(kLseThreads, 1)
     }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], kLseRedThreads);
+      // every reduction thread reads every tile with a mask; half of them
+      // (the group of the tile's parity) without
+      mbar_init(&s_free[s], a.has_mask ? kLseRedThreads : kLseRedThreads / 2);
     }
     mbar_init(final_bar, 1);
     fence_barrier_init();
@@ -321,9 +367,18 @@ __global__ void __launch_bounds__(kLseThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ reduction
-    const int sp = warp & 3, quarter = (warp - 4) >> 2;
+    // Without a mask the 16 warps form two groups that take alternate key
+    // tiles (group = tile parity), each thread covering half of a tile's
+    // columns, so one group's TMEM loads overlap the other group's arithmetic.
+    // With a mask every warp reads every tile, a quarter of its columns, and
+    // the quarter's mask values are requested before the wait for the scores.
+    const int sp = warp & 3, w4 = warp - 4;
     const int r = sp * 32 + lane;  // query row of the item (TMEM lane)
-    const uint32_t t_row = tmem + ((uint32_t)(sp * 32) << 16) + quarter * QC;
+    const bool split = !a.has_mask;
+    const int grp = split ? (w4 >> 3) : 0;
+    const int part = split ? ((w4 >> 2) & 1) : (w4 >> 2);  // column share of the tile
+    const int ncol = split ? QC2 : QC;
+    const uint32_t t_row = tmem + ((uint32_t)(sp * 32) << 16) + part * ncol;
     const float c = a.scale_log2e;
     const uint64_t c2 = lse_pk2(c, c), one2 = lse_pk2(1.f, 1.f);
     int g = 0;
@@ -347,90 +402,90 @@ __global__ void __launch_bounds__(kLseThreads, 1)
         lo = (int)l0;
         hi = (int)h0;
       }
-      const float* mrow = a.has_mask && q_ok ? a.mask + (long long)it.b * a.msb +
-                                                   (long long)it.h * a.msh + (long long)q * a.msq
-                                             : nullptr;
       float m = -INFINITY, l = 0.f;
-      for (int t = 0; ok && t < it.T; ++t, ++g) {
-        const int sb = g % NSB;
-        const int kb = it.k_start + t * BN + quarter * QC;  // first key of this thread's share
-        // the share's mask values, requested before the wait for the scores
-        float mv[QC];
+      if (split) {
+        for (int t = 0; ok && t < it.T; ++t, ++g) {
+          if ((g & 1) != grp) continue;
+          const int sb = g % NSB;
+          const int kb = it.k_start + t * BN + part * QC2;  // first key of this share
+          if (!warp_wait_all(&s_full[sb], (g / NSB) & 1, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sv[QC2];
+          __syncwarp();
 #pragma unroll
-        for (int e = 0; e < QC; ++e) mv[e] = 0.f;
-        if (mrow && kb < hi && kb + QC > lo) {
-          if (a.mask_vec) {
+          for (int c0 = 0; c0 < QC2; c0 += 16) {
+            uint32_t rr[16];
+            tmem_ld16(t_row + sb * BN + c0, rr);
 #pragma unroll
-            for (int e = 0; e < QC; e += 4) {
-              if (kb + e + 4 <= a.Sk) {
-                const float4 v4 = __ldg(reinterpret_cast<const float4*>(mrow + kb + e));
-                mv[e] = v4.x;
-                mv[e + 1] = v4.y;
-                mv[e + 2] = v4.z;
-                mv[e + 3] = v4.w;
-              } else {
+            for (int e = 0; e < 16; ++e) sv[c0 + e] = rr[e];
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&s_free[sb]);
+          lse_share<QC2, false>(sv, sv, kb, lo, hi, c, c2, one2, m, l);
+        }
+      } else {
+        const float* mrow = q_ok ? a.mask + (long long)it.b * a.msb + (long long)it.h * a.msh +
+                                       (long long)q * a.msq
+                                 : nullptr;
+        for (int t = 0; ok && t < it.T; ++t, ++g) {
+          const int sb = g % NSB;
+          const int kb = it.k_start + t * BN + part * QC;  // first key of this share
+          // the share's mask values, requested before the wait for the scores
+          float mv[QC];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (kb + e + u < a.Sk) mv[e + u] = __ldg(mrow + kb + e + u);
+          for (int e = 0; e < QC; ++e) mv[e] = 0.f;
+          if (mrow && kb < hi && kb + QC > lo) {
+            if (a.mask_vec) {
+#pragma unroll
+              for (int e = 0; e < QC; e += 4) {
+                if (kb + e + 4 <= a.Sk) {
+                  const float4 v4 = __ldg(reinterpret_cast<const float4*>(mrow + kb + e));
+                  mv[e] = v4.x;
+                  mv[e + 1] = v4.y;
+                  mv[e + 2] = v4.z;
+                  mv[e + 3] = v4.w;
+                } else {
+#pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    if (kb + e + u < a.Sk) mv[e + u] = __ldg(mrow + kb + e + u);
+                }
               }
+            } else {
+#pragma unroll
+              for (int e = 0; e < QC; ++e)
+                if (kb + e < a.Sk) mv[e] = __ldg(mrow + (long long)(kb + e) * a.msk);
             }
-          } else {
-#pragma unroll
-            for (int e = 0; e < QC; ++e)
-              if (kb + e < a.Sk) mv[e] = __ldg(mrow + (long long)(kb + e) * a.msk);
           }
-        }
-        if (!warp_wait_all(&s_full[sb], (g / NSB) & 1, a.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sv[QC];
-        __syncwarp();
-#pragma unroll
-        for (int c0 = 0; c0 < QC; c0 += 16) {
-          uint32_t rr[16];
-          tmem_ld16(t_row + sb * BN + c0, rr);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sv[c0 + e] = rr[e];
-        }
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&s_free[sb]);
-        // the share's keys against this row's visible interval [lo, hi):
-        // none visible (skip), all visible without a mask (scores only), or
-        // per key
-        if (kb >= hi || kb + QC <= lo) continue;
-        if (!mrow && kb >= lo && kb + QC <= hi) {
-          float sf[QC];
-#pragma unroll
-          for (int e = 0; e < QC; ++e) sf[e] = __uint_as_float(sv[e]);
-          // max of s * c is c * (max s), or c * (min s) for a negative scale
-          const float mx = c >= 0.f ? tree_ext<QC, true>(sf) * c : tree_ext<QC, false>(sf) * c;
-          const float mn = fmaxf(m, mx);
-          const float sum = sum_ex2<QC>(sf, c2, lse_pk2(-mn, -mn));
-          l = fmaf(l, lse_ex2(m - mn), sum);
-          m = mn;
-        } else {
-          float x[QC];
-#pragma unroll
-          for (int e = 0; e < QC; ++e) {
-            const bool vis = (unsigned)(kb + e - lo) < (unsigned)(hi - lo) && mv[e] > kHardMask;
-            x[e] = vis ? fmaf(__uint_as_float(sv[e]), c, mv[e] * kLog2e) : -INFINITY;
+          if (!warp_wait_all(&s_full[sb], (g / NSB) & 1, a.err)) {
+            ok = false;
+            break;
           }
-          const float mn = fmaxf(m, tree_ext<QC, true>(x));
-          if (mn != -INFINITY) {
-            const float sum = sum_ex2<QC>(x, one2, lse_pk2(-mn, -mn));
-            l = fmaf(l, lse_ex2(m - mn), sum);
-            m = mn;
+          tc_fence_after();
+          uint32_t sv[QC];
+          __syncwarp();
+#pragma unroll
+          for (int c0 = 0; c0 < QC; c0 += 16) {
+            uint32_t rr[16];
+            tmem_ld16(t_row + sb * BN + c0, rr);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[c0 + e] = rr[e];
           }
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&s_free[sb]);
+          lse_share<QC, true>(sv, mv, kb, lo, hi, c, c2, one2, m, l);
         }
       }
-      // merge the four quarters of each row; every reduction thread arrives
-      // at both barriers, also after a failed wait
-      red[quarter * BM + r] = make_float2(m, l);
+      // merge the four partial (m, l) of each row; every reduction thread
+      // arrives at both barriers, also after a failed wait
+      const int q4 = split ? grp * 2 + part : part;
+      red[q4 * BM + r] = make_float2(m, l);
       red_sync();
-      if (quarter == 0) {
+      if (q4 == 0) {
         float2 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) v[u] = red[u * BM + r];

@@ -33,6 +33,13 @@ def counted_flops(p) -> float:
     return 10.0 * p.head_dim * pairs * p.batch * p.num_heads
 
 
+def lse_flops(p) -> float:
+    """2 * D flops per visible pair per query head (the score product of the
+    LSE sweep), over the whole batch."""
+    pairs = visible_pairs(p.seq_q, p.seq_k, p.causal, p.causal_offset, p.window)
+    return 2.0 * p.head_dim * pairs * p.batch * p.num_heads
+
+
 def decode_bytes(p) -> int:
     """Minimum HBM bytes of the decode backward: K and V history read once per
     sequence (shared by the query heads of a KV head), probs and d_out read,

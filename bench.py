@@ -34,6 +34,7 @@ from attention_backward_pass_gb300 import metrics as MET  # noqa: E402
 from attention_backward_pass_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attention-backward TFLOP/s (dQ+dK+dV) and % of GB300 dense tensor peak"
+LSE_METRIC = "LSE sweep TFLOP/s (2*D flops per visible pair) and % of GB300 dense tensor peak"
 L2_BYTES = 129 * 1024 * 1024
 # nominal dense ratio TF32 : BF16 on GB300 (1.1 vs 2.25 PFLOP/s)
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -65,6 +66,10 @@ def parse_args():
     ap.add_argument("--workload", default="causal_mha", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute-lse", action="store_true",
+                    help="dense workloads: the step recomputes the LSE (attn_bwd_lse) first")
+    ap.add_argument("--lse-only", action="store_true",
+                    help="dense workloads: time the LSE sweep (attn_bwd_lse) alone")
     return ap.parse_args()
 
 
@@ -345,9 +350,13 @@ def run_ours(args):
     ws = ab.alloc_workspace(p, device)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
+    rec = args.recompute_lse
+    lse_buf = torch.empty_like(x["LSE"]) if rec else x["LSE"]
 
     def step():
-        ab.attn_bwd(p, x["Q"], x["K"], x["V"], x["O"], x["dO"], x["LSE"], x["mask"], dQ, dK, dV,
+        if rec:
+            ab.attn_bwd_lse(p, x["Q"], x["K"], x["mask"], lse_buf)
+        ab.attn_bwd(p, x["Q"], x["K"], x["V"], x["O"], x["dO"], lse_buf, x["mask"], dQ, dK, dV,
                     ws)
 
     for _ in range(max(args.warmup, 3)):
@@ -356,7 +365,7 @@ def run_ours(args):
     if ab.check_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     load_under_clock_sampling(step)
     if world > 1:
@@ -365,8 +374,11 @@ def run_ours(args):
     for k in range(args.steps):
         flush.zero_()  # L2 flush between timed steps (outside the events)
         e = evs[k]
+        e[4].record(stream)
+        if rec:  # no saved LSE: the sweep is part of the step
+            ab.attn_bwd_lse(p, x["Q"], x["K"], x["mask"], lse_buf)
         e[0].record(stream)
-        ab.attn_bwd_prepare(p, x["Q"], x["K"], x["O"], x["dO"], x["LSE"], dQ, ws)
+        ab.attn_bwd_prepare(p, x["Q"], x["K"], x["O"], x["dO"], lse_buf, dQ, ws)
         e[1].record(stream)
         ab.attn_bwd_tiles(p, x["Q"], x["K"], x["V"], x["dO"], x["mask"], dQ, dK, dV, ws)
         e[2].record(stream)
@@ -378,7 +390,8 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     if ab.check_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[4].elapsed_time(e[3]) for e in evs]
+    lse_ms = [e[4].elapsed_time(e[0]) for e in evs]
     tile_ms = [e[1].elapsed_time(e[2]) for e in evs]
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = sum(step_ms)
@@ -423,15 +436,116 @@ def run_ours(args):
             "dtype": "bf16" if p.dtype == W.DTYPE_BF16 else "tf32",
             "data": "synthetic",
             "config": {"workload": desc, "l2": "flushed between timed steps (256 MiB write)",
-                       "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+                       "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                       "lse": ("recomputed in the step by attn_bwd_lse (its 2*D flops per "
+                               "visible pair are not counted)") if rec else "given"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": "dkdv_kernel (tcgen05 tile kernel)", "peak_source": peak_note,
-                         "kernel_ms": tile_mean, "prep_ms": statistics.mean(prep_ms)},
+                         "kernel_ms": tile_mean, "prep_ms": statistics.mean(prep_ms),
+                         "lse_ms": statistics.mean(lse_ms) if rec else 0.0},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": ab.kernels_per_call(p) * args.steps,
+            "gpu_launches": ab.kernels_per_call(p, recompute_lse=rec) * args.steps,
             "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_lse_only(args):
+    """The LSE sweep alone (attn_bwd_lse) on a dense workload: tensor-bound,
+    value = 2*D flops per visible pair / time."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    ab.load_library()
+    make, seed, desc = WORKLOADS[args.workload]
+    p = make()
+    Qn, Kn, _, _, maskn = W.make_inputs(p, seed)
+    tdt = torch.bfloat16 if p.dtype == W.DTYPE_BF16 else torch.float32
+    Q = torch.from_numpy(Qn).to(device).to(tdt)
+    K = torch.from_numpy(Kn).to(device).to(tdt)
+    mask = torch.from_numpy(maskn).to(device) if maskn is not None else None
+    lse = torch.empty(p.lse_shape(), dtype=torch.float32, device=device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ab.attn_bwd_lse(p, Q, K, mask, lse)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    load_under_clock_sampling(step)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set")
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total = sum(ms)
+    if world > 1:
+        t = torch.tensor([total], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    flops = MET.lse_flops(p)
+    value = flops * world * args.steps / (total * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    if p.dtype == W.DTYPE_BF16:
+        peak, note = bf16_peak, f"bf16 dense, {src} burst"
+    else:
+        peak, note = bf16_peak * TF32_OVER_BF16, f"tf32 dense = {src} bf16 burst x nominal 1.1/2.25"
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import attention as OA
+        groups_all = [(b, g) for b in range(p.batch) for g in range(p.num_kv_heads)]
+        t0 = time.perf_counter()
+        done = 0
+        for grp in groups_all:
+            OA.lse(p, Qn.astype(np.float64), Kn.astype(np.float64), maskn, groups=[grp])
+            done += 1
+            if time.perf_counter() - t0 > 12.0:
+                break
+        secs = time.perf_counter() - t0
+        cpu = {"value": flops / len(groups_all) * done / secs / 1e12, "unit": "TFLOP/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{done} of {len(groups_all)} (batch, kv-head) groups, {secs:.1f} s, "
+                         "fp64 numpy"}
+    if rank == 0:
+        mean_ms = statistics.mean(ms)
+        line = {
+            "metric": LSE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if p.dtype == W.DTYPE_BF16 else "tf32", "data": "synthetic",
+            "config": {"workload": "LSE sweep of " + desc,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12,
+                         "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
+                         "traffic": read_traffic(args.workload, prefix="lse_"),
+                         "kernel": "lse_kernel (persistent tcgen05)", "peak_source": note},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -442,7 +556,8 @@ def run_ours(args):
 def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
     import torch
     import attention_backward_pass_gb300 as ab
-    names = ["Q", "K", "V", "O", "dO", "LSE"] + (["mask"] if x["mask"] is not None else [])
+    names = (["Q", "K", "V", "O", "dO"] + ([] if args.recompute_lse else ["LSE"])
+             + (["mask"] if x["mask"] is not None else []))
     host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in names}
     for k in names:
         host[k].copy_(x[k])
@@ -457,8 +572,8 @@ def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
         evs[i][0].record(stream)
         for k in names:
             dev[k].copy_(host[k], non_blocking=True)
-        ab.attn_bwd(p, dev["Q"], dev["K"], dev["V"], dev["O"], dev["dO"], dev["LSE"],
-                    dev.get("mask"), dQ, dK, dV, ws)
+        ab.attn_bwd(p, dev["Q"], dev["K"], dev["V"], dev["O"], dev["dO"],
+                    None if args.recompute_lse else dev["LSE"], dev.get("mask"), dQ, dK, dV, ws)
         for t_h, t_d in zip(outs_h, (dQ, dK, dV)):
             t_h.copy_(t_d, non_blocking=True)
         evs[i][1].record(stream)
@@ -603,6 +718,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.lse_only and args.workload not in ("decode", "decode_kv"):
+        return run_lse_only(args)
     if args.workload in ("decode", "decode_kv"):
         return run_decode(args)
     return run_ours(args)
