@@ -81,6 +81,23 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest x over all ranks (the slowest rank's time), or x itself when
+    no process group is running.  Every rank must call it."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, steps: int, total_ms: float) -> float:
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return units_per_rank * world * steps / (total_ms * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -395,12 +412,9 @@ def run_ours(args):
     tile_ms = [e[1].elapsed_time(e[2]) for e in evs]
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device)
     flops = MET.counted_flops(p)
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, args.steps, total_ms) / 1e12
     ms_per_step = total_ms / args.steps
 
     # roofline of the dominant kernel (the fused tile kernel)
@@ -502,12 +516,9 @@ def run_lse_only(args):
         raise RuntimeError("device error word set")
     ms = [a.elapsed_time(b) for a, b in evs]
     total = sum(ms)
-    if world > 1:
-        t = torch.tensor([total], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
+    total = max_over_ranks(total, device)
     flops = MET.lse_flops(p)
-    value = flops * world * args.steps / (total * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, args.steps, total) / 1e12
     peaks, src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
     if p.dtype == W.DTYPE_BF16:
@@ -579,10 +590,7 @@ def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in evs[2:]) / n
-    if world > 1:
-        t = torch.tensor([ms], device=dQ.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dQ.device)
     value = MET.counted_flops(p) * world / (ms * 1e-3) / 1e12
     return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
@@ -663,12 +671,9 @@ def run_decode(args):
         raise RuntimeError("device error word set")
     ms = [a.elapsed_time(b) for a, b in evs]
     total = sum(ms)
-    if world > 1:
-        tt = torch.tensor([total], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total = float(tt.item())
+    total = max_over_ranks(total, device)
     nbytes = MET.decode_kv_bytes(p) if kv_pass else MET.decode_bytes(p)
-    value = nbytes * world * args.steps / (total * 1e-3) / 1e9
+    value = whole_job_rate(nbytes, world, args.steps, total) / 1e9
     peaks, src = load_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
     cpu = None
