@@ -43,6 +43,7 @@ class AttnBwdParams(ctypes.Structure):
         ("mask_stride_b", ctypes.c_int64), ("mask_stride_h", ctypes.c_int64),
         ("mask_stride_q", ctypes.c_int64), ("mask_stride_k", ctypes.c_int64),
         ("layout", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("deterministic", ctypes.c_int32),
     ]
 
 
@@ -132,7 +133,8 @@ def make_params(p) -> AttnBwdParams:
                          float(p.scale), float(p.dropout_prob), int(p.seed) & (2**64 - 1),
                          int(p.causal), int(p.causal_offset), int(p.window), int(p.has_mask),
                          int(p.mask_stride_b), int(p.mask_stride_h), int(p.mask_stride_q),
-                         int(p.mask_stride_k), int(p.layout), int(p.dtype))
+                         int(p.mask_stride_k), int(p.layout), int(p.dtype),
+                         int(getattr(p, "deterministic", 0)))
 
 
 def workspace_size(p) -> int:
@@ -198,8 +200,10 @@ def attn_bwd_lse(p, Q, K, mask, LSE, stream=None):
 
 def kernels_per_call(p, recompute_lse: bool = False) -> int:
     """Kernels one attn_bwd call launches (the LSE sweep when no LSE is
-    given, prepare, tile kernel, and for bf16 the dQ conversion)."""
-    return (1 if recompute_lse else 0) + 1 + 1 + (1 if p.dtype == ATTN_BF16 else 0)
+    given, prepare, tile kernel, and the finishing kernel: bf16 dQ conversion,
+    or the ordered dQ reduction when deterministic)."""
+    finish = 1 if (p.dtype == ATTN_BF16 or getattr(p, "deterministic", 0)) else 0
+    return (1 if recompute_lse else 0) + 1 + 1 + finish
 
 
 def make_decode_params(p) -> AttnBwdDecodeParams:

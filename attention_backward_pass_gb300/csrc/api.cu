@@ -59,6 +59,7 @@ attn_status validate(const attn_bwd_params* p) {
   if (p->causal != 0 && p->causal != 1) return ATTN_ERR_INVALID;
   if (p->causal_offset < 0 || p->window < 0) return ATTN_ERR_INVALID;
   if (p->has_mask != 0 && p->has_mask != 1) return ATTN_ERR_INVALID;
+  if (p->deterministic != 0 && p->deterministic != 1) return ATTN_ERR_INVALID;
   // row and element counts must fit the kernels' index arithmetic
   const long long rows_q = (long long)p->batch * p->num_heads * p->seq_q;
   const long long rows_k = (long long)p->batch * p->num_kv_heads * p->seq_k;
@@ -68,6 +69,7 @@ attn_status validate(const attn_bwd_params* p) {
   if ((long long)p->batch * p->num_heads >= (1LL << 31) / 1024) return ATTN_ERR_INVALID;
   const long long kv_tiles = (p->seq_k + 63) / 64;  // smallest key tile
   if (kv_tiles * p->batch * p->num_kv_heads >= (1LL << 31)) return ATTN_ERR_INVALID;
+  if (p->deterministic && kv_tiles * rows_q * p->head_dim >= (1LL << 40)) return ATTN_ERR_INVALID;
   return ATTN_OK;
 }
 
@@ -76,8 +78,10 @@ attn_status validate(const attn_bwd_params* p) {
 //   dq_acc        fp32 dQ accumulator (bf16 only; fp32 accumulates in dQ)
 //   qt, dot, kt   transposed fp32 copies [B*H][D][sq_pad], [B*Hkv][D][sk_pad]
 //                 (fp32 only: TF32 products take K-major operands)
+//   dqp           deterministic dQ: one fp32 slice per key tile,
+//                 [n_kv_tiles * B][H][Sq][D]
 struct WsLayout {
-  size_t delta, lse2, dq_acc, qt, dot, kt, total;
+  size_t delta, lse2, dq_acc, qt, dot, kt, dqp, total;
   int sq_pad, sk_pad;
 };
 
@@ -97,7 +101,14 @@ WsLayout ws_layout(const attn_bwd_params& p) {
   w.kt = w.dot + qt;
   const size_t kt =
       bf ? 0 : align256((size_t)p.batch * p.num_kv_heads * w.sk_pad * p.head_dim * 4);
-  w.total = w.kt + kt;
+  w.dqp = w.kt + kt;
+  size_t dqp = 0;
+  if (p.deterministic) {
+    const size_t n_kt = (size_t)((p.seq_k + dkdv_block_n(p.dtype, p.head_dim) - 1) /
+                                 dkdv_block_n(p.dtype, p.head_dim));
+    dqp = align256(n_kt * p.batch * p.num_heads * p.seq_q * p.head_dim * 4);
+  }
+  w.total = w.dqp + dqp;
   return w;
 }
 
@@ -232,7 +243,7 @@ namespace {
 
 struct Plan {
   WsLayout wl;
-  float *delta, *lse2, *dq_acc, *qt, *dot, *kt;
+  float *delta, *lse2, *dq_acc, *qt, *dot, *kt, *dqp;
 };
 
 attn_status make_plan(const attn_bwd_params* p, void* dQ, void* workspace, size_t workspace_bytes,
@@ -252,6 +263,7 @@ attn_status make_plan(const attn_bwd_params* p, void* dQ, void* workspace, size_
   pl->qt = reinterpret_cast<float*>(ws + pl->wl.qt);
   pl->dot = reinterpret_cast<float*>(ws + pl->wl.dot);
   pl->kt = reinterpret_cast<float*>(ws + pl->wl.kt);
+  pl->dqp = reinterpret_cast<float*>(ws + pl->wl.dqp);
   return ATTN_OK;
 }
 
@@ -378,8 +390,12 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
                bn) != CUDA_SUCCESS ||
       make_map(&maps.v, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
                bn) != CUDA_SUCCESS ||
-      make_map_dq(&maps.dq, pl.dq_acc, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
-                  dkdv_dq_box_d(p->dtype, p->head_dim), bm) != CUDA_SUCCESS)
+      (p->deterministic
+           ? make_map_dq(&maps.dq, pl.dqp, p->head_dim, p->seq_q, p->num_heads,
+                         p->batch * ((p->seq_k + bn - 1) / bn), ATTN_LAYOUT_BHSD,
+                         dkdv_dq_box_d(p->dtype, p->head_dim), bm)
+           : make_map_dq(&maps.dq, pl.dq_acc, p->head_dim, p->seq_q, p->num_heads, p->batch,
+                         p->layout, dkdv_dq_box_d(p->dtype, p->head_dim), bm)) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
 
   TileArgs a;
@@ -411,7 +427,8 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
   a.seed_hi = (uint32_t)(p->seed >> 32);
   a.lse2 = pl.lse2;
   a.delta = pl.delta;
-  a.dq_acc = pl.dq_acc;
+  a.dq_acc = p->deterministic ? pl.dqp : pl.dq_acc;
+  a.det = p->deterministic;
   a.dK = dK;
   a.dV = dV;
   a.n_kv_tiles = (p->seq_k + bn - 1) / bn;
@@ -425,10 +442,15 @@ attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
   Plan pl;
   attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
   if (st != ATTN_OK) return st;
-  if (p->dtype == ATTN_BF16 &&
-      launch_dq_convert(*p, pl.dq_acc, dQ, reinterpret_cast<cudaStream_t>(stream_v)) !=
-          cudaSuccess)
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  if (p->deterministic) {
+    if (launch_dq_reduce(*p, pl.dqp, dQ, dkdv_block_n(p->dtype, p->head_dim),
+                         dkdv_block_m(p->dtype, p->head_dim), stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  } else if (p->dtype == ATTN_BF16 &&
+             launch_dq_convert(*p, pl.dq_acc, dQ, stream) != cudaSuccess) {
     return ATTN_ERR_CUDA;
+  }
   return ATTN_OK;
 }
 

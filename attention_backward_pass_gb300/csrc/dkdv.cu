@@ -1096,7 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(dq_free);
       const int nq = min(BM, a.Sq - q0);
-      float* gbase = a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
+      // deterministic: this key tile's own dQ slice, [kt * B + b][h][q][d]
+      const int kt = w.k0 / BN;
+      float* gbase = a.det ? a.dq_acc + row_offset(0, kt * a.B + w.b, h, q0, a.H, a.Sq, D)
+                           : a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
       if constexpr (L::DQT) {
         // stage [BM queries][STG d] and hand the tile to the TMA engine as one
         // reduce-add (rows past Sq fall outside the tensor map and are skipped)
@@ -1112,7 +1115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           dq_group_sync();
           if (tid == 0) {
-            tma_reduce_add_4d(&tm_dq, stg, d0, q0, h, w.b);
+            if (a.det)
+              tma_store_4d(&tm_dq, stg, d0, q0, h, kt * a.B + w.b);
+            else
+              tma_reduce_add_4d(&tm_dq, stg, d0, q0, h, w.b);
             bulk_commit();
           }
         }
@@ -1121,10 +1127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // dQ: row r = query of the tile, columns = d (already contiguous)
         if (r >= 0 && r < nq) {
-          float4* dst = reinterpret_cast<float4*>(gbase + r * rstride);
+          float4* dst = reinterpret_cast<float4*>(gbase + r * (a.det ? D : rstride));
+          if (a.det) {
 #pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+            for (int c = 0; c < D / 4; ++c)
+              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c)
+              atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          }
         }
       }
     }

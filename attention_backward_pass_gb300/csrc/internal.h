@@ -33,7 +33,9 @@ struct TileArgs {
   uint32_t seed_lo, seed_hi;
   const float* lse2;   // [B*H][sq_pad]  -LSE * log2(e), -inf in padding rows
   const float* delta;  // [B*H][sq_pad]  rowsum(dO * O), 0 in padding rows
-  float* dq_acc;       // fp32 dQ accumulator, same layout as dQ (dQ itself for fp32)
+  float* dq_acc;       // fp32 dQ accumulator, same layout as dQ (dQ itself for fp32);
+                       // deterministic: the per-key-tile slices [n_kv_tiles*B][H][Sq][D]
+  int det;             // 1: store dQ slices instead of adding into dq_acc
   void* dK;
   void* dV;
   int n_kv_tiles;
@@ -82,6 +84,10 @@ cudaError_t launch_prep(const attn_bwd_params& p, const void* O, const void* dO,
                         cudaStream_t stream);
 cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, void* dQ,
                               cudaStream_t stream);
+// Deterministic dQ: dQ = sum over key tiles kt (ascending) of slice kt, over
+// the query tiles the dK/dV CTA of kt visited (block sizes bn x bm).
+cudaError_t launch_dq_reduce(const attn_bwd_params& p, const float* slices, void* dQ, int bn,
+                             int bm, cudaStream_t stream);
 
 struct TileMaps {
   CUtensorMap q, k, v, dout;  // natural [.., S, .., D] tensors

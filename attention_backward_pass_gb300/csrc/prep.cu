@@ -240,6 +240,111 @@ cudaError_t launch_prep_f32(const attn_bwd_params& p, const float* Q, const floa
   return cudaGetLastError();
 }
 
+namespace {
+
+// Deterministic dQ: one group of G = D/4 threads per dQ row (b, h, q), one
+// float4 each; the row is the sum, in ascending key-tile order, of the slices
+// of the key tiles whose dK/dV CTA visited the row's query tile (the same
+// query ranges as the tile kernel's, so unvisited slices, which hold no data,
+// are never read).  Per round of G key tiles every thread of the group tests
+// one tile, a ballot hands the group the visited set, and the group then
+// loads up to four slices before adding them, in order.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) dq_reduce_kernel(const float* __restrict__ slices,
+                                                        void* __restrict__ dQ, int B, int H,
+                                                        int Sq, int Sk, int layout, int causal,
+                                                        long long off, long long window, int bn,
+                                                        int bm, int n_kt) {
+  constexpr int G = D / 4;           // threads per row (16 or 32)
+  constexpr int ROWS = 256 / G;      // rows per block
+  const long long row = (long long)blockIdx.x * ROWS + threadIdx.x / G;
+  const int sub = threadIdx.x % G;
+  const int lane = threadIdx.x & 31;
+  const long long nrows = (long long)B * H * Sq;
+  const bool row_ok = row < nrows;  // every lane stays for the ballots
+  const long long rr = row_ok ? row : 0;
+  const int q = (int)(rr % Sq);
+  const int bh = (int)(rr / Sq);
+  const int b = bh / H, h = bh % H;
+  const float4* base = reinterpret_cast<const float4*>(slices) + sub;
+  const long long kt_stride = (long long)B * H * Sq * (D / 4);  // float4 per slice
+  const long long row4 = (((long long)b * H + h) * Sq + q) * (D / 4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](const float4& v) {
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  };
+  for (int kt0 = 0; kt0 < n_kt; kt0 += G) {
+    const int kt = kt0 + sub;
+    bool vis = false;
+    if (row_ok && kt < n_kt) {
+      const long long k0 = (long long)kt * bn;
+      const long long k1 = (k0 + bn < Sk ? k0 + bn : Sk) - 1;
+      int qb = 0, qe = 0;
+      query_range(Sq, causal, off, window, k0, k1, &qb, &qe);
+      if (qe > qb) {
+        const int q_first = (qb / bm) * bm;
+        const int tiles = (qe - q_first + bm - 1) / bm;
+        vis = q >= q_first && q < q_first + tiles * bm;
+      }
+    }
+    unsigned bits = __ballot_sync(0xffffffffu, vis);
+    if constexpr (G < 32) bits = (bits >> (lane & ~(G - 1))) & ((1u << G) - 1u);
+    while (bits) {
+      int j[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        j[u] = bits ? __ffs(bits) - 1 : -1;
+        bits &= bits ? bits - 1 : 0u;
+      }
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j[u] >= 0) v[u] = base[(long long)(kt0 + j[u]) * kt_stride + row4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j[u] >= 0) add(v[u]);
+    }
+  }
+  if (!row_ok) return;
+  const long long o = row_offset(layout, b, h, q, H, Sq, D) + 4 * sub;
+  if constexpr (BF16) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dQ) + o) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(dQ) + o) = acc;
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t dq_reduce_impl(const attn_bwd_params& p, const float* slices, void* dQ, int bn,
+                           int bm, cudaStream_t stream) {
+  constexpr int ROWS = 256 / (D / 4);
+  const long long nrows = (long long)p.batch * p.num_heads * p.seq_q;
+  const long long blocks = (nrows + ROWS - 1) / ROWS;
+  const int n_kt = (p.seq_k + bn - 1) / bn;
+  dq_reduce_kernel<BF16, D><<<(unsigned)blocks, 256, 0, stream>>>(
+      slices, dQ, p.batch, p.num_heads, p.seq_q, p.seq_k, p.layout, p.causal, p.causal_offset,
+      p.window, bn, bm, n_kt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dq_reduce(const attn_bwd_params& p, const float* slices, void* dQ, int bn,
+                             int bm, cudaStream_t stream) {
+  const bool bf = p.dtype == ATTN_BF16;
+  if (p.head_dim == 64)
+    return bf ? dq_reduce_impl<true, 64>(p, slices, dQ, bn, bm, stream)
+              : dq_reduce_impl<false, 64>(p, slices, dQ, bn, bm, stream);
+  return bf ? dq_reduce_impl<true, 128>(p, slices, dQ, bn, bm, stream)
+            : dq_reduce_impl<false, 128>(p, slices, dQ, bn, bm, stream);
+}
+
 cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, void* dQ,
                               cudaStream_t stream) {
   const long long n4 = (long long)p.batch * p.num_heads * p.seq_q * p.head_dim / 4;

@@ -148,6 +148,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
       : "memory");
 }
 
+// 4-D tiled store shared -> global (bulk group); elements outside the tensor
+// are not written.  Coordinates must not be negative.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // 4-D tiled reduce-add shared -> global through TMA (bulk group), and its
 // completion controls.  The shared source must keep its contents until
 // bulk_wait_read() returns.

@@ -51,6 +51,7 @@ class AttnProblem:
     mask_stride_k: int = 0
     layout: int = LAYOUT_BHSD
     dtype: int = DTYPE_F32
+    deterministic: int = 0
 
     def q_shape(self):
         if self.layout == LAYOUT_BHSD:

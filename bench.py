@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--recompute-lse", action="store_true",
                     help="dense workloads: the step recomputes the LSE (attn_bwd_lse) first")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="dense workloads: bit-reproducible dQ (per-key-tile slices, ordered sum)")
     ap.add_argument("--lse-only", action="store_true",
                     help="dense workloads: time the LSE sweep (attn_bwd_lse) alone")
     return ap.parse_args()
@@ -359,6 +361,7 @@ def run_ours(args):
     ab.load_library()
     make, seed, desc = WORKLOADS[args.workload]
     p = make()
+    p.deterministic = 1 if args.deterministic else 0
     x = device_inputs(p, seed, device)
     tdt = x["Q"].dtype
     dQ = torch.empty(p.q_shape(), dtype=tdt, device=device)
@@ -452,7 +455,9 @@ def run_ours(args):
             "config": {"workload": desc, "l2": "flushed between timed steps (256 MiB write)",
                        "flops_per_step": flops, "parallelism": f"replicas x{world}",
                        "lse": ("recomputed in the step by attn_bwd_lse (its 2*D flops per "
-                               "visible pair are not counted)") if rec else "given"},
+                               "visible pair are not counted)") if rec else "given",
+                       "dq": ("deterministic: per-key-tile slices summed in key-tile order"
+                              if p.deterministic else "fp32 reduce-add (atomic)")},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": "dkdv_kernel (tcgen05 tile kernel)", "peak_source": peak_note,

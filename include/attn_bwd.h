@@ -93,11 +93,14 @@ typedef struct {
   int64_t mask_stride_k;
   int32_t layout; /* attn_layout */
   int32_t dtype;  /* attn_dtype */
+  int32_t deterministic; /* 0/1: dQ reproducible bit for bit (see attn_bwd) */
 } attn_bwd_params;
 
 /*
  * Bytes of device workspace attn_bwd needs for `p` (0 only if p is invalid).
- * Holds per-row Delta and LSE*log2(e) and, for bf16, the fp32 dQ accumulator.
+ * Holds per-row Delta and LSE*log2(e) and, for bf16, the fp32 dQ accumulator;
+ * with p->deterministic also one fp32 dQ slice per key tile,
+ * ceil(seq_k / key tile) * batch * num_heads * seq_q * head_dim * 4 bytes.
  */
 size_t attn_bwd_workspace_size(const attn_bwd_params* p);
 
@@ -116,8 +119,12 @@ size_t attn_bwd_workspace_size(const attn_bwd_params* p);
  *   workspace: device memory of >= attn_bwd_workspace_size(p) bytes, 256-byte
  *        aligned; its contents on entry do not matter.
  * Every tensor pointer must be 16-byte aligned (TMA).  Tensors are dense in the
- * stated layout.  dQ accumulation uses fp32 atomics, so dQ can differ in the
- * last bits from run to run; dK and dV are deterministic.
+ * stated layout.  By default dQ accumulation uses fp32 atomics, so dQ can
+ * differ in the last bits from run to run; dK and dV are deterministic.  With
+ * p->deterministic every key tile writes its dQ contribution to its own
+ * workspace slice and a final kernel sums the slices in key-tile order (the
+ * WGSL page's dQ pass is atomic-free for the same reason), so dQ is the same
+ * bit for bit on every run, at the cost of that workspace and its traffic.
  * Errors: ATTN_ERR_INVALID (null/misaligned pointer, bad sizes, bad dropout_prob,
  * mask pointer/has_mask mismatch), ATTN_ERR_UNSUPPORTED (head_dim), ATTN_ERR_WORKSPACE,
  * ATTN_ERR_CUDA.
@@ -138,7 +145,9 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
  *                    the tensor-core products read.
  *  attn_bwd_tiles    the fused tile kernel: recomputes P, forms dS and
  *                    produces dK, dV and the dQ accumulation.
- *  attn_bwd_finish   bf16 only: converts the fp32 dQ accumulator to dQ.
+ *  attn_bwd_finish   bf16: converts the fp32 dQ accumulator to dQ; with
+ *                    p->deterministic (either dtype): sums the per-key-tile
+ *                    dQ slices in key-tile order into dQ.
  */
 attn_status attn_bwd_prepare(const attn_bwd_params* p, const void* Q, const void* K,
                              const void* O, const void* dO, const float* LSE, void* dQ,

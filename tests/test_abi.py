@@ -93,6 +93,22 @@ def test_null_pointers_and_mask_mismatch(lib):
     assert lib.attn_bwd(ctypes.byref(prm), *args, ctypes.c_void_p(4096 + 16), 1 << 30, None) == -5
 
 
+def test_deterministic_workspace_and_flag(lib):
+    # one fp32 dQ slice per key tile (128 keys for fp32 D=64) on top of the
+    # usual workspace; any flag value other than 0 / 1 is rejected
+    p = W.causal_mha()
+    n0 = ab.workspace_size(p)
+    p.deterministic = 1
+    n1 = ab.workspace_size(p)
+    n_kt = (p.seq_k + 127) // 128
+    assert n1 - n0 == n_kt * p.batch * p.num_heads * p.seq_q * p.head_dim * 4
+    p.deterministic = 2
+    assert lib.attn_bwd_workspace_size(ctypes.byref(ab.make_params(p))) == 0
+    assert ab.kernels_per_call(W.causal_mha()) == 2
+    p.deterministic = 1
+    assert ab.kernels_per_call(p) == 3
+
+
 def test_workspace_sizes(lib):
     for p in (W.tiny(), W.causal_mha(), W.gqa_window(W.DTYPE_BF16), W.masked_dropout()):
         n = ab.workspace_size(p)
