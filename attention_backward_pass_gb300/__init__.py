@@ -67,6 +67,9 @@ _SIGS = {
     "attn_bwd_finish": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, ctypes.c_size_t,
                                        _P]),
     "attn_bwd_lse": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P]),
+    "attn_fwd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdParams)]),
+    "attn_fwd": (ctypes.c_int, [ctypes.POINTER(AttnBwdParams), _P, _P, _P, _P, _P, _P, _P,
+                                ctypes.c_size_t, _P]),
     "attn_bwd_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnBwdDecodeParams)]),
     "attn_bwd_decode": (ctypes.c_int, [ctypes.POINTER(AttnBwdDecodeParams), _P, _P, _P, _P, _P,
                                        _P, _P, ctypes.c_size_t, _P]),
@@ -196,6 +199,22 @@ def attn_bwd_lse(p, Q, K, mask, LSE, stream=None):
     st = load_library().attn_bwd_lse(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(mask),
                                      _ptr(LSE), _stream_ptr(stream))
     _check("attn_bwd_lse", st)
+
+
+def fwd_workspace_size(p) -> int:
+    lib = load_library()
+    n = lib.attn_fwd_workspace_size(ctypes.byref(make_params(p)))
+    if n == 0:
+        raise AttnError("attn_fwd_workspace_size", -1)
+    return int(n)
+
+
+def attn_fwd(p, Q, K, V, mask, O, LSE, workspace, stream=None):
+    """Fused forward: O (p's layout and dtype) and LSE [B, H, Sq] (fp32)."""
+    st = load_library().attn_fwd(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(V),
+                                 _ptr(mask), _ptr(O), _ptr(LSE), _ptr(workspace),
+                                 _wsb(workspace), _stream_ptr(stream))
+    _check("attn_fwd", st)
 
 
 def kernels_per_call(p, recompute_lse: bool = False) -> int:

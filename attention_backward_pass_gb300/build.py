@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattnbwd.so")
 
-SOURCES = ["api.cu", "prep.cu", "dkdv.cu", "decode.cu", "lse.cu", "selftest.cu"]
+SOURCES = ["api.cu", "prep.cu", "dkdv.cu", "decode.cu", "lse.cu", "fwd.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -478,6 +478,76 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
   return attn_bwd_finish(p, dQ, workspace, workspace_bytes, stream);
 }
 
+size_t attn_fwd_workspace_size(const attn_bwd_params* p) {
+  if (validate(p) != ATTN_OK) return 0;
+  if (p->dtype == ATTN_BF16) return 256;  // not used
+  return align256((size_t)p->batch * p->num_kv_heads * round_up(p->seq_k, kRowPad) *
+                  p->head_dim * 4);
+}
+
+attn_status attn_fwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                     const float* mask, void* O, float* LSE, void* workspace,
+                     size_t workspace_bytes, void* stream_v) {
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (!all_aligned({Q, K, V, O, LSE})) return ATTN_ERR_INVALID;
+  if ((p->has_mask != 0) != (mask != nullptr)) return ATTN_ERR_INVALID;
+  const size_t need = attn_fwd_workspace_size(p);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  const int bn = fwd_block_n(p->dtype, p->head_dim);
+  const int sk_pad = round_up(p->seq_k, kRowPad);
+  CUtensorMap tq, tk, tv;
+  if (make_map(&tq, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
+               128) != CUDA_SUCCESS ||
+      make_map(&tk, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
+               bn) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  if (p->dtype == ATTN_BF16) {
+    if (make_map(&tv, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
+                 bn) != CUDA_SUCCESS)
+      return ATTN_ERR_CUDA;
+  } else {
+    // fp32: V^T [B*Hkv][D][sk_pad], TF32-rounded, in the workspace
+    float* vt = reinterpret_cast<float*>(workspace);
+    if (launch_transpose_kv_f32(*p, static_cast<const float*>(V), vt, sk_pad, stream) !=
+            cudaSuccess ||
+        make_map_t(&tv, vt, p->head_dim, p->seq_k, sk_pad, p->batch * p->num_kv_heads) !=
+            CUDA_SUCCESS)
+      return ATTN_ERR_CUDA;
+  }
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.B = p->batch;
+  a.H = p->num_heads;
+  a.group = p->num_heads / p->num_kv_heads;
+  a.Sq = p->seq_q;
+  a.Sk = p->seq_k;
+  a.layout = p->layout;
+  a.scale_log2e = p->scale * kLog2e;
+  a.causal = p->causal;
+  a.causal_offset = p->causal_offset;
+  a.window = p->window;
+  a.has_mask = p->has_mask;
+  a.msb = p->mask_stride_b;
+  a.msh = p->mask_stride_h;
+  a.msq = p->mask_stride_q;
+  a.msk = p->mask_stride_k;
+  a.mask = mask;
+  a.dropout = p->dropout_prob > 0.f ? 1 : 0;
+  a.drop_threshold = dropout_threshold(p->dropout_prob);
+  a.drop_inv_keep = (float)(1.0 / (1.0 - (double)p->dropout_prob));
+  a.seed_lo = (uint32_t)(p->seed & 0xFFFFFFFFu);
+  a.seed_hi = (uint32_t)(p->seed >> 32);
+  a.O = O;
+  a.LSE = LSE;
+  a.err = err;
+  return launch_fwd(*p, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 static attn_status validate_decode(const attn_bwd_decode_params* p) {
   if (!p) return ATTN_ERR_INVALID;
   if (p->num_seqs < 1 || p->n_heads < 1 || p->n_kv_heads < 1 || p->history_len < 1)

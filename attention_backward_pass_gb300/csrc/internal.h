@@ -135,6 +135,33 @@ struct LseArgs {
   float* out;
   unsigned int* err;
 };
+// Fused forward (O and LSE) on the tensor cores.
+struct FwdArgs {
+  int B, H, group, Sq, Sk, layout;
+  float scale_log2e;  // scale * log2(e)
+  int causal;
+  long long causal_offset, window;
+  int has_mask;
+  long long msb, msh, msq, msk;
+  const float* mask;
+  int dropout;              // 0 / 1
+  uint32_t drop_threshold;  // keep iff philox word >= threshold
+  float drop_inv_keep;      // 1 / (1 - p)
+  uint32_t seed_lo, seed_hi;
+  void* O;     // [B,H,Sq,D] or [B,Sq,H,D], the problem's dtype
+  float* LSE;  // [B*H][Sq]
+  unsigned int* err;
+};
+// tq: Q, boxes of 128 rows; tk: K, boxes of fwd_block_n rows; tv: V (bf16,
+// boxes of fwd_block_n rows) or V^T [B*Hkv][D][sk_pad] (fp32, boxes of 32 keys
+// x D rows).
+int fwd_block_n(int dtype, int head_dim);
+cudaError_t launch_fwd(const attn_bwd_params& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream);
+// fp32 V^T [B*Hkv][D][sk_pad], TF32-rounded (the key side of the fp32 prepare).
+cudaError_t launch_transpose_kv_f32(const attn_bwd_params& p, const float* X, float* xt,
+                                    int sk_pad, cudaStream_t stream);
+
 constexpr float kHardMask = -1.0e30f;     // a mask value at or below this hides the pair
 constexpr float kEmptyRowLse = 3.0e38f;   // LSE of a row with no probability mass
 // tq: Q in the problem's layout, boxes of 128 rows; tk: K, boxes of

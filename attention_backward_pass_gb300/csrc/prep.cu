@@ -345,6 +345,23 @@ cudaError_t launch_dq_reduce(const attn_bwd_params& p, const float* slices, void
             : dq_reduce_impl<false, 128>(p, slices, dQ, bn, bm, stream);
 }
 
+cudaError_t launch_transpose_kv_f32(const attn_bwd_params& p, const float* X, float* xt,
+                                    int sk_pad, cudaStream_t stream) {
+  // key-side blocks of the fp32 prepare only (no query-side blocks)
+  const int nk = p.batch * p.num_kv_heads * (sk_pad / 32);
+  if (p.head_dim == 64)
+    prep_f32_kernel<64><<<nk, 256, 0, stream>>>(nullptr, X, nullptr, nullptr, nullptr, nullptr,
+                                                nullptr, nullptr, nullptr, nullptr, xt, p.batch,
+                                                p.num_heads, p.num_kv_heads, p.seq_q, p.seq_k, 0,
+                                                sk_pad, p.layout, 0);
+  else
+    prep_f32_kernel<128><<<nk, 256, 0, stream>>>(nullptr, X, nullptr, nullptr, nullptr, nullptr,
+                                                 nullptr, nullptr, nullptr, nullptr, xt, p.batch,
+                                                 p.num_heads, p.num_kv_heads, p.seq_q, p.seq_k, 0,
+                                                 sk_pad, p.layout, 0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, void* dQ,
                               cudaStream_t stream) {
   const long long n4 = (long long)p.batch * p.num_heads * p.seq_q * p.head_dim / 4;

@@ -177,6 +177,27 @@ attn_status attn_bwd_lse(const attn_bwd_params* p, const void* Q, const void* K,
                          const float* mask, float* LSE, void* stream);
 
 /*
+ * Fused forward pass, producing the backward's inputs on the GPU with the same
+ * conventions (the WGSL page's forward is referenced by its backward but not
+ * printed; read as the function whose gradients attn_bwd computes):
+ *   s_ij  = scale * Q_i . K_j + mask_ij   on visible pairs with mask_ij > -1e30
+ *   LSE_i = log sum_j exp(s_ij)           (3e38 for a row with no such pair)
+ *   O_i   = sum_j exp(s_ij - LSE_i) M_ij V_j
+ * with M the dropout multiplier of attn_bwd (same Philox4x32-10 stream, keep
+ * mask identical to attn_dropout_keep_mask), and O_i = 0 for an empty row.
+ *   Q, K, V: p->layout, p->dtype; fp32 inputs are multiplied as TF32.
+ *   mask: as for attn_bwd.  O: p->layout, p->dtype (written).  LSE: fp32
+ *   [B, H, Sq] (written).  workspace: >= attn_fwd_workspace_size(p) bytes,
+ *   256-byte aligned (fp32: a TF32 copy of V^T).
+ * Device pointers, 16-byte aligned.  p->deterministic is ignored (the forward
+ * has no atomics).  Errors as for attn_bwd.
+ */
+size_t attn_fwd_workspace_size(const attn_bwd_params* p);
+attn_status attn_fwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                     const float* mask, void* O, float* LSE, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * Decode (one query per head) backward, pass 1 of the decode page
  * ("rullama attention_backward_dq.wgsl"): probabilities are given and the
  * scores were unscaled, kv = h / (n_heads / n_kv_heads):

@@ -155,6 +155,23 @@ def run_lse_gpu(p, Q, K, mask, device="cuda"):
     return out.cpu().numpy().astype(np.float64)
 
 
+def run_fwd_gpu(p, Q, K, V, mask, device="cuda"):
+    """attn_fwd through the C ABI; returns fp64 numpy O (p's layout) and LSE."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    q = _torch_io(Q, p.dtype, device)
+    k = _torch_io(K, p.dtype, device)
+    v = _torch_io(V, p.dtype, device)
+    m = torch.from_numpy(mask).to(device) if mask is not None else None
+    o = torch.full(p.q_shape(), float("nan"), dtype=q.dtype, device=device)
+    lse = torch.full((p.batch, p.num_heads, p.seq_q), float("nan"), device=device)
+    ws = torch.empty(ab.fwd_workspace_size(p), dtype=torch.uint8, device=device)
+    ab.attn_fwd(p, q, k, v, m, o, lse, ws)
+    torch.cuda.synchronize()
+    assert ab.check_device_error() == 0
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
 def decode_case(p, seed):
     k, v, d_out, logits = W.make_decode_inputs(p, seed)
     probs = OD.softmax_rows(logits).astype(np.float32)

@@ -93,6 +93,25 @@ def test_null_pointers_and_mask_mismatch(lib):
     assert lib.attn_bwd(ctypes.byref(prm), *args, ctypes.c_void_p(4096 + 16), 1 << 30, None) == -5
 
 
+def test_forward_validation(lib):
+    prm = ab.make_params(P())
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    # null or misaligned tensors, mask pointer without has_mask, small workspace
+    assert lib.attn_fwd(ctypes.byref(prm), None, fake, fake, None, fake, fake, ws, 1 << 30,
+                        None) == -1
+    assert lib.attn_fwd(ctypes.byref(prm), fake, fake, ctypes.c_void_p(4100), None, fake, fake,
+                        ws, 1 << 30, None) == -1
+    assert lib.attn_fwd(ctypes.byref(prm), fake, fake, fake, fake, fake, fake, ws, 1 << 30,
+                        None) == -1
+    assert lib.attn_fwd(ctypes.byref(prm), fake, fake, fake, None, fake, fake, ws, 16,
+                        None) == -5
+    # fp32 needs a TF32 copy of V^T; bf16 needs no workspace to speak of
+    p = W.causal_mha()
+    assert ab.fwd_workspace_size(p) == p.batch * p.num_kv_heads * 1024 * p.head_dim * 4
+    assert ab.fwd_workspace_size(W.gqa_window(W.DTYPE_BF16)) == 256
+
+
 def test_deterministic_workspace_and_flag(lib):
     # one fp32 dQ slice per key tile (128 keys for fp32 D=64) on top of the
     # usual workspace; any flag value other than 0 / 1 is rejected
