@@ -35,6 +35,7 @@ from attention_backward_pass_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attention-backward TFLOP/s (dQ+dK+dV) and % of GB300 dense tensor peak"
 LSE_METRIC = "LSE sweep TFLOP/s (2*D flops per visible pair) and % of GB300 dense tensor peak"
+FWD_METRIC = "attention-forward TFLOP/s (4*D flops per visible pair) and % of GB300 dense tensor peak"
 L2_BYTES = 129 * 1024 * 1024
 # nominal dense ratio TF32 : BF16 on GB300 (1.1 vs 2.25 PFLOP/s)
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -70,6 +71,8 @@ def parse_args():
                     help="dense workloads: the step recomputes the LSE (attn_bwd_lse) first")
     ap.add_argument("--deterministic", action="store_true",
                     help="dense workloads: bit-reproducible dQ (per-key-tile slices, ordered sum)")
+    ap.add_argument("--fwd", action="store_true",
+                    help="dense workloads: time the fused forward (attn_fwd) instead")
     ap.add_argument("--lse-only", action="store_true",
                     help="dense workloads: time the LSE sweep (attn_bwd_lse) alone")
     return ap.parse_args()
@@ -569,6 +572,106 @@ def run_lse_only(args):
     return 0
 
 
+def run_fwd(args):
+    """The fused forward (attn_fwd) on a dense workload: tensor-bound,
+    value = 4*D flops per visible pair (S = Q K^T and O = P V) / time."""
+    import torch
+    import attention_backward_pass_gb300 as ab
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    ab.load_library()
+    make, seed, desc = WORKLOADS[args.workload]
+    p = make()
+    Qn, Kn, Vn, _, maskn = W.make_inputs(p, seed)
+    tdt = torch.bfloat16 if p.dtype == W.DTYPE_BF16 else torch.float32
+    Q, K, V = (torch.from_numpy(a).to(device).to(tdt) for a in (Qn, Kn, Vn))
+    mask = torch.from_numpy(maskn).to(device) if maskn is not None else None
+    O = torch.empty(p.q_shape(), dtype=tdt, device=device)
+    lse = torch.empty(p.lse_shape(), dtype=torch.float32, device=device)
+    ws = torch.empty(ab.fwd_workspace_size(p), dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ab.attn_fwd(p, Q, K, V, mask, O, lse, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    load_under_clock_sampling(step)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set")
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total = max_over_ranks(sum(ms), device)
+    flops = 2.0 * MET.lse_flops(p)  # 2*D for S, 2*D for P V
+    value = whole_job_rate(flops, world, args.steps, total) / 1e12
+    peaks, src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    if p.dtype == W.DTYPE_BF16:
+        peak, note = bf16_peak, f"bf16 dense, {src} burst"
+    else:
+        peak, note = bf16_peak * TF32_OVER_BF16, f"tf32 dense = {src} bf16 burst x nominal 1.1/2.25"
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import attention as OA
+        groups_all = [(b, g) for b in range(p.batch) for g in range(p.num_kv_heads)]
+        f = lambda a: a.astype(np.float64)  # noqa: E731
+        t0 = time.perf_counter()
+        done = 0
+        for grp in groups_all:
+            OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=[grp])
+            done += 1
+            if time.perf_counter() - t0 > 12.0:
+                break
+        secs = time.perf_counter() - t0
+        cpu = {"value": flops / len(groups_all) * done / secs / 1e12, "unit": "TFLOP/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{done} of {len(groups_all)} (batch, kv-head) groups, {secs:.1f} s, "
+                         "fp64 numpy"}
+    if rank == 0:
+        mean_ms = statistics.mean(ms)
+        line = {
+            "metric": FWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if p.dtype == W.DTYPE_BF16 else "tf32", "data": "synthetic",
+            "config": {"workload": "forward of " + desc,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12,
+                         "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
+                         "traffic": read_traffic(args.workload, prefix="fwd_"),
+                         "kernel": "fwd_kernel (persistent tcgen05)", "peak_source": note},
+            "cpu_baseline": cpu, "e2e": None,
+            "gpu_launches": (1 if p.dtype == W.DTYPE_BF16 else 2) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
     import torch
     import attention_backward_pass_gb300 as ab
@@ -730,6 +833,8 @@ def main():
         return run_reference(args)
     if args.lse_only and args.workload not in ("decode", "decode_kv"):
         return run_lse_only(args)
+    if args.fwd and args.workload not in ("decode", "decode_kv"):
+        return run_fwd(args)
     if args.workload in ("decode", "decode_kv"):
         return run_decode(args)
     return run_ours(args)
