@@ -321,14 +321,29 @@ def run_reference(args):
     Qn, Kn, Vn, dOn, maskn = W.make_inputs(p, seed)
     f = lambda x: x.astype(np.float64)  # noqa: E731
     groups_all = [(b, g) for b in range(p.batch) for g in range(p.num_kv_heads)]
-    per_group = MET.counted_flops(p) / len(groups_all)
+    # the same work as the arm being compared: the LSE sweep, the forward, or
+    # the backward (default)
+    if args.lse_only:
+        metric, flops = LSE_METRIC, MET.lse_flops(p)
+    elif args.fwd:
+        metric, flops = FWD_METRIC, 2.0 * MET.lse_flops(p)
+    else:
+        metric, flops = METRIC, MET.counted_flops(p)
+    per_group = flops / len(groups_all)
     vals = []
     rng = np.random.default_rng(0)
     for step in range(args.warmup + args.steps):
         grp = [groups_all[int(rng.integers(len(groups_all)))]]
-        O, LSE = OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)  # untimed inputs
-        t0 = time.perf_counter()
-        OA.backward(p, f(Qn), f(Kn), f(Vn), O, f(dOn), LSE, maskn, groups=grp)
+        if args.lse_only:
+            t0 = time.perf_counter()
+            OA.lse(p, f(Qn), f(Kn), maskn, groups=grp)
+        elif args.fwd:
+            t0 = time.perf_counter()
+            OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)
+        else:
+            O, LSE = OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)  # untimed inputs
+            t0 = time.perf_counter()
+            OA.backward(p, f(Qn), f(Kn), f(Vn), O, f(dOn), LSE, maskn, groups=grp)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             vals.append(per_group / dt / 1e12)
@@ -336,7 +351,7 @@ def run_reference(args):
     cores = os.cpu_count()
     sample = f"one (batch, kv-head) group of {len(groups_all)} per step, fp64 numpy"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_group / (value * 1e12) * 1e3 * len(groups_all),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
