@@ -106,7 +106,7 @@ __device__ __forceinline__ uint32_t fwd_pack_bf16(float lo, float hi) {
 
 // Keys [k_start, k_end) that a row of [q0, q1] can see; k_start rounded down
 // to a multiple of 16 so that mask rows can be read as float4 (the same range
-// rule as the LSE sweep).
+// rule as the LSE sweep); an empty range stays empty (no tile is loaded).
 __device__ __forceinline__ void fwd_key_range(const FwdArgs& a, int q0, int q1, int* ks,
                                               int* ke) {
   const long long qa_min = (long long)q0 + a.causal_offset;
@@ -117,7 +117,11 @@ __device__ __forceinline__ void fwd_key_range(const FwdArgs& a, int q0, int q1, 
     if (qa_min - a.window + 1 > lo) lo = qa_min - a.window + 1;
     if (!a.causal && qa_max + a.window < hi) hi = qa_max + a.window;
   }
-  if (hi < lo) hi = lo;
+  if (hi <= lo) {
+    *ks = 0;
+    *ke = 0;
+    return;
+  }
   lo &= ~15LL;
   *ks = (int)lo;
   *ke = (int)hi;
