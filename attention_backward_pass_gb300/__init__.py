@@ -17,6 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libattnbwd.so")
 
 ATTN_OK = 0
+ATTN_ERR_TIMEOUT = -4
 STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
                 -3: "CUDA error", -4: "device wait timed out", -5: "workspace problem",
                 -6: "problem exceeds the fixed no-allocation scratch array"}
@@ -83,6 +84,7 @@ _SIGS = {
                                             ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
                                             ctypes.POINTER(ctypes.c_int32)]),
     "attn_bwd_check_device_error": (ctypes.c_int, [ctypes.c_int32]),
+    "attn_selftest_wait_timeout": (ctypes.c_int, [_P]),
     "attn_selftest_mma": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, _P, _P, _P, _P, _P]),
@@ -285,6 +287,12 @@ def query_range(p, k0, k1):
                                   ctypes.byref(qe))
     _check("attn_bwd_query_range", st)
     return qb.value, qe.value
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the failure-path self test (a wait that runs out)."""
+    _check("attn_selftest_wait_timeout",
+           load_library().attn_selftest_wait_timeout(_stream_ptr(stream)))
 
 
 def check_device_error(clear: bool = True) -> int:

@@ -637,6 +637,10 @@ attn_status attn_bwd_check_device_error(int32_t clear_it) {
   return v == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
 
+attn_status attn_selftest_wait_timeout(void* stream) {
+  return selftest_wait_launch(reinterpret_cast<cudaStream_t>(stream));
+}
+
 attn_status attn_selftest_mma(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t a_mn,
                               int32_t b_mn, int32_t a_tmem, const void* A, const void* B,
                               float* C, float* tmem_dump, void* stream) {

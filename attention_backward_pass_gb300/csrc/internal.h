@@ -74,6 +74,7 @@ __host__ __device__ __forceinline__ void query_range(int Sq, int causal, long lo
 
 unsigned int* device_error_word();
 
+attn_status selftest_wait_launch(cudaStream_t stream);
 attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, int a_tmem,
                                 const void* A, const void* B, float* C, float* dump,
                                 cudaStream_t stream);

@@ -163,7 +163,28 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
+// Failure-path hook: one thread waits on an mbarrier that nothing ever
+// arrives on.  The library's bounded wait gives up after about a second, raises
+// the device error word and returns, so the kernel ends normally.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(unsigned int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err);
+  __syncwarp();
+}
+
 }  // namespace
+
+attn_status selftest_wait_launch(cudaStream_t stream) {
+  unsigned int* err = device_error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, int a_tmem,
                                 const void* A, const void* B, float* C, float* dump,

@@ -323,6 +323,16 @@ attn_status attn_selftest_mma(int32_t dtype, int32_t M, int32_t N, int32_t K, in
                               int32_t b_mn, int32_t a_tmem, const void* A, const void* B,
                               float* C, float* tmem_dump, void* stream);
 
+/*
+ * Failure-path self test: enqueues one tiny kernel whose single wait can never
+ * be satisfied (an mbarrier nothing arrives on).  The bounded wait every
+ * kernel of the library uses gives up after about a second and raises the
+ * device error word; after synchronising, attn_bwd_check_device_error reports
+ * ATTN_ERR_TIMEOUT (and clears the word if asked), and the context stays
+ * usable.  No trap, no fault, no hang.
+ */
+attn_status attn_selftest_wait_timeout(void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status s);
 
