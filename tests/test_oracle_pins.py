@@ -133,6 +133,73 @@ def test_against_torch_autograd(name):
         np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
 
 
+def strided_mask(p, kind, seed):
+    """A logical additive mask L [B, H, Sq, Sk] (N(0,1) values, 20 % at the
+    -1e30 sentinel, every head different) and the storage the oracle reads
+    through p's element strides:
+      per_head            [B, H, Sq, Sk]   strides (H Sq Sk, Sq Sk, Sk, 1)
+      per_head_transposed [B, H, Sk, Sq]   strides (H Sq Sk, Sq Sk, 1, Sq)
+      head_major          [H, B, Sk, Sq]   strides (Sq Sk, B Sq Sk, 1, Sq)
+    Sets the strides on p and returns (storage, L)."""
+    rng = np.random.default_rng(seed)
+    B, H, Sq, Sk = p.batch, p.num_heads, p.seq_q, p.seq_k
+    L = rng.standard_normal((B, H, Sq, Sk))
+    L[rng.random(L.shape) < 0.2] = W.MASKED
+    if kind == "per_head":
+        store = L.copy()
+        strides = (H * Sq * Sk, Sq * Sk, Sk, 1)
+    elif kind == "per_head_transposed":
+        store = np.ascontiguousarray(L.transpose(0, 1, 3, 2))
+        strides = (H * Sq * Sk, Sq * Sk, 1, Sq)
+    elif kind == "head_major":
+        store = np.ascontiguousarray(L.transpose(1, 0, 3, 2))
+        strides = (Sq * Sk, B * Sq * Sk, 1, Sq)
+    else:
+        raise ValueError(kind)
+    p.has_mask = 1
+    p.mask_stride_b, p.mask_stride_h, p.mask_stride_q, p.mask_stride_k = strides
+    return store, L
+
+
+@pytest.mark.parametrize("kind", ["per_head", "per_head_transposed", "head_major"])
+def test_strided_per_head_mask_against_torch_autograd(kind):
+    """The mask is indexed with the query head (not its KV head) and with the
+    q / k strides the caller gives (page 2, fab2_mask_at).  GQA with two query
+    heads per KV head, two batches and a different mask per (b, h): a head
+    index taken from the KV head, a swapped q / k stride or a dropped batch
+    term reads another head's or the transposed values and fails here."""
+    p = small(batch=2, num_heads=4, num_kv_heads=2, seq_q=5, seq_k=7, causal=1,
+              causal_offset=3, layout=W.LAYOUT_BSHD, dropout_prob=0.2, seed=31)
+    Q, K, V, dO, _ = inputs64(p, seed=9)
+    store, L = strided_mask(p, kind, seed=17)
+    M = np.stack([np.stack([A.multiplier(p, b, h) for h in range(p.num_heads)])
+                  for b in range(p.batch)])
+    o_t, lse_t, dq_t, dk_t, dv_t = _torch_reference(p, Q, K, V, dO, L, M)
+    O, LSE = A.forward(p, Q, K, V, store)
+    dQ, dK, dV = A.backward(p, Q, K, V, O, dO, LSE, store)
+    np.testing.assert_allclose(O, o_t, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(LSE, lse_t, rtol=1e-12, atol=1e-12)
+    for a, b in ((dQ, dq_t), (dK, dk_t), (dV, dv_t)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+    # the LSE sweep reads the mask the same way
+    np.testing.assert_allclose(A.lse(p, Q, K, store), lse_t, rtol=1e-12, atol=1e-12)
+
+
+def test_mask_head_stride_reaches_every_query_head():
+    """Brute force on the index rule alone: with a per-head mask that holds
+    the flat element index, mask_slice returns b*sb + h*sh + i*sq + j*sk."""
+    p = small(batch=2, num_heads=6, num_kv_heads=2, seq_q=3, seq_k=4, has_mask=1)
+    sb, sh, sq, sk = 97, 13, 1, 3
+    p.mask_stride_b, p.mask_stride_h, p.mask_stride_q, p.mask_stride_k = sb, sh, sq, sk
+    flat = np.arange(2 * 97 + 6 * 13 + 10, dtype=np.float64)
+    for b in range(p.batch):
+        for h in range(p.num_heads):
+            got = A.mask_slice(p, flat, b, h)
+            for i in range(p.seq_q):
+                for j in range(p.seq_k):
+                    assert got[i, j] == b * sb + h * sh + i * sq + j * sk
+
+
 @pytest.mark.parametrize("name", ["plain", "causal_window_offset", "mask", "dropout",
                                   "everything"])
 def test_invariants(name):
