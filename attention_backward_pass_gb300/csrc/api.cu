@@ -21,6 +21,7 @@ __device__ unsigned int g_error_word_storage = 0u;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+void* g_err_ctx[kMaxDevices] = {nullptr};  // context the cached address belongs to
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -203,14 +204,37 @@ CUresult make_f32_map(CUtensorMap* m, const void* base, int rank, const long lon
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Handle of the driver context current on this thread (nullptr if none or
+// if the driver entry point is unavailable).  The device addresses of the
+// library's __device__ variables belong to that context: after
+// cudaDeviceReset the runtime creates a new primary context, in which they
+// are loaded again at other addresses.
+void* current_context() {
+  using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return reinterpret_cast<void*>(ctx);
+}
+
 unsigned int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
+  if (!g_err_ptr[dev] || g_err_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_error_word_storage) != cudaSuccess) return nullptr;
     g_err_ptr[dev] = reinterpret_cast<unsigned int*>(ptr);
+    g_err_ctx[dev] = current_context();  // the lookup created it if there was none
   }
   return g_err_ptr[dev];
 }

@@ -1102,17 +1102,23 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / 
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kNoAllocMaxDevices] = {nullptr};
+void* g_noalloc_ctx[kNoAllocMaxDevices] = {nullptr};  // context of the cached address
 
-// Device address of the scratch array for the current device (nullptr on error).
+// Device address of the scratch array for the current device (nullptr on
+// error).  Looked up on the first call with the device current, and again
+// whenever the device's context has changed since (after cudaDeviceReset
+// the array lives at another address in the new context).
 float* noalloc_scratch_for_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
     float* ptr = nullptr;
     if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
       return nullptr;
     g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ctx[dev] = current_context();  // the lookup created it if there was none
   }
   return g_noalloc_ptr[dev];
 }

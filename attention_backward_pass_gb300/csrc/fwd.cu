@@ -412,33 +412,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int u = 1; u < 4; ++u) mt = fmaxf(mt, rmax[((g & 1) * 4 + u) * BM + r]);
         // lazy rescale: raise m only when the tile's maximum exceeds it by
-        // more than 2^8 (the same decision in all four threads of a row)
+        // more than 2^8 (the same decision in all four threads of a row).
+        // The decision is per row, i.e. per lane, so the rescale of O below
+        // (warp-collective TMEM accesses and a warp-wide wait) runs for the
+        // whole warp whenever any lane needs it, with factor 1 in the others.
+        float f = 1.f;
         if (mt != -INFINITY) {
           if (m == -INFINITY) {
             m = mt;  // no mass so far: O and l are zero
           } else if (mt > m + kRescaleLog2) {
-            const float f = fwd_ex2(m - mt);
+            f = fwd_ex2(m - mt);
             l *= f;
             m = mt;
-            if (t > 0 && ok) {
-              // O *= f on this thread's D/4 columns, after the previous P . V
-              const int gp = g - 1;
-              ok = fwd_warp_wait(&pv_done[gp % NSB], (gp / NSB) & 1, a.err);
-              if (ok) {
-                tc_fence_after();
-                __syncwarp();
+          }
+        }
+        if (t > 0 && ok && __any_sync(0xffffffffu, f != 1.f)) {
+          // O *= f on this thread's D/4 columns, after the previous P . V
+          const int gp = g - 1;
+          ok = fwd_warp_wait(&pv_done[gp % NSB], (gp / NSB) & 1, a.err);
+          if (ok) {
+            tc_fence_after();
+            __syncwarp();
 #pragma unroll
-                for (int c0 = 0; c0 < OC; c0 += 16) {
-                  uint32_t ov[16];
-                  tmem_ld16(tmem + lane_base + L::T_O + part * OC + c0, ov);
-                  tmem_ld_wait();
+            for (int c0 = 0; c0 < OC; c0 += 16) {
+              uint32_t ov[16];
+              tmem_ld16(tmem + lane_base + L::T_O + part * OC + c0, ov);
+              tmem_ld_wait();
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-                  tmem_st16(tmem + lane_base + L::T_O + part * OC + c0, ov);
-                }
-                tmem_st_wait();
-              }
+              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+              tmem_st16(tmem + lane_base + L::T_O + part * OC + c0, ov);
             }
+            tmem_st_wait();
           }
         }
         // dropout keep bits of the share (bit e: key kb + e), one Philox4x32-10

@@ -73,6 +73,8 @@ __host__ __device__ __forceinline__ void query_range(int Sq, int causal, long lo
 }
 
 unsigned int* device_error_word();
+// Driver context current on this thread (opaque handle; nullptr if none).
+void* current_context();
 
 attn_status selftest_wait_launch(cudaStream_t stream);
 attn_status selftest_mma_launch(int dtype, int M, int N, int K, int a_mn, int b_mn, int a_tmem,

@@ -12,6 +12,7 @@ the workload on its own GPU (weak scaling, no collective on the data path);
 the reported value is the work of all ranks over the slowest rank's time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  (default workload: GQA causal + window 1024, B2 Hq32 Hkv8 S4096 D128, fp32 I/O on TF32)
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
 """
 from __future__ import annotations
@@ -64,7 +65,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="causal_mha", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="gqa_window_f32", choices=sorted(WORKLOADS),
+                    help="default: the GQA causal + sliding-window workload at fp32 I/O (TF32), "
+                         "the largest dense configuration")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--recompute-lse", action="store_true",
@@ -84,6 +87,66 @@ def load_peaks():
         with open(path) as f:
             return json.load(f), "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def measure_matmul_peak(device, dtype_name="tf32", n=8192, reps=10, sustain_s=2.0):
+    """Dense tensor-core peak of this GPU for one operand type, measured the
+    way the bf16 figures of MEASURED_PEAKS.json are: torch.matmul of n x n x n
+    (2 n^3 flops), CUDA events, best of ``reps`` back-to-back products
+    (burst) and the mean rate over ``sustain_s`` seconds of back-to-back
+    products (sustained).  tf32 = fp32 tensors with TF32 tensor-op math.
+    Returns (burst TFLOP/s, sustained TFLOP/s)."""
+    import torch
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = dtype_name == "tf32"
+    try:
+        dt = torch.float32 if dtype_name == "tf32" else torch.bfloat16
+        g = torch.Generator(device=device).manual_seed(0)
+        a = torch.randn(n, n, device=device, dtype=dt, generator=g)
+        b = torch.randn(n, n, device=device, dtype=dt, generator=g)
+        c = torch.empty(n, n, device=device, dtype=dt)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        flops = 2.0 * n ** 3
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        count = 0
+        t0 = time.perf_counter()
+        e0.record()
+        while time.perf_counter() - t0 < sustain_s:
+            for _ in range(10):
+                torch.matmul(a, b, out=c)
+            count += 10
+            e1.record()
+            e1.synchronize()
+        sustained = flops * count / (e0.elapsed_time(e1) * 1e-3) / 1e12
+        del a, b, c
+        return flops / (best * 1e-3) / 1e12, sustained
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+
+
+def tensor_peak(p, device, peaks, peak_src):
+    """(peak TFLOP/s, description, extra fields) for the tile kernels' operand
+    type: bf16 from MEASURED_PEAKS.json (burst), TF32 measured in this run
+    with measure_matmul_peak (burst), with the nominal-ratio figure kept
+    beside it for comparison."""
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    if p.dtype == W.DTYPE_BF16:
+        return bf16_peak, f"bf16 dense, {peak_src} burst (MEASURED_PEAKS.json)", {}
+    burst, sustained = measure_matmul_peak(device, "tf32")
+    extra = {"tf32_burst_tflops": burst, "tf32_sustained_tflops": sustained,
+             "tf32_nominal_ratio_tflops": bf16_peak * TF32_OVER_BF16}
+    return burst, ("tf32 dense, measured in this run: torch.matmul fp32 with TF32 math, "
+                   "8192^3, best of 10 (burst)"), extra
 
 
 def max_over_ranks(x: float, device="cpu") -> float:
@@ -291,13 +354,14 @@ def run_reference_decode(args):
             OD.decode_backward(k, v, probs, d_out, seqs=[n])
         dt = time.perf_counter() - t0
         if step >= args.warmup:
-            vals.append(per_seq / dt / 1e9)
-    value = statistics.mean(vals)
-    sample = f"one sequence of {p.num_seqs} per step, fp64 numpy"
+            vals.append(dt)
+    value = per_seq * len(vals) / sum(vals) / 1e9
+    sample = (f"one sequence of {p.num_seqs} per step, fp64 numpy; ms_per_step is the time of "
+              "that one sequence")
     line = {
         "impl": "reference", "metric": DECODE_KV_METRIC if kv_pass else DECODE_METRIC,
         "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": nbytes / (value * 1e9) * 1e3,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(vals) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": desc, "sample": sample},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
@@ -330,33 +394,45 @@ def run_reference(args):
     else:
         metric, flops = METRIC, MET.counted_flops(p)
     per_group = flops / len(groups_all)
-    vals = []
+    vals, secs = [], []
+    # fp64 copies made once, outside the timed calls; steps cycle over (at
+    # most) four seeded groups, whose O / LSE inputs are synthesised once
+    Q64, K64, V64, dO64 = f(Qn), f(Kn), f(Vn), f(dOn)
     rng = np.random.default_rng(0)
+    picks = [groups_all[int(i)] for i in rng.permutation(len(groups_all))[:4]]
+    fwd_cache = {}
     for step in range(args.warmup + args.steps):
-        grp = [groups_all[int(rng.integers(len(groups_all)))]]
+        grp = [picks[step % len(picks)]]
         if args.lse_only:
             t0 = time.perf_counter()
-            OA.lse(p, f(Qn), f(Kn), maskn, groups=grp)
+            OA.lse(p, Q64, K64, maskn, groups=grp)
         elif args.fwd:
             t0 = time.perf_counter()
-            OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)
+            OA.forward(p, Q64, K64, V64, maskn, groups=grp)
         else:
-            O, LSE = OA.forward(p, f(Qn), f(Kn), f(Vn), maskn, groups=grp)  # untimed inputs
+            if grp[0] not in fwd_cache:  # untimed input synthesis
+                fwd_cache[grp[0]] = OA.forward(p, Q64, K64, V64, maskn, groups=grp)
+            O, LSE = fwd_cache[grp[0]]
             t0 = time.perf_counter()
-            OA.backward(p, f(Qn), f(Kn), f(Vn), O, f(dOn), LSE, maskn, groups=grp)
+            OA.backward(p, Q64, K64, V64, O, dO64, LSE, maskn, groups=grp)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             vals.append(per_group / dt / 1e12)
-    value = statistics.mean(vals)
+            secs.append(dt)
+    # value: the work timed (one group per step) over the time it took
+    value = per_group * len(secs) / sum(secs) / 1e12
     cores = os.cpu_count()
-    sample = f"one (batch, kv-head) group of {len(groups_all)} per step, fp64 numpy"
+    sample = (f"one (batch, kv-head) group of {len(groups_all)} per step "
+              f"({per_group / 1e9:.2f} GFLOP counted), fp64 numpy; ms_per_step is the time of "
+              "that one group")
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_group / (value * 1e12) * 1e3 * len(groups_all),
+        "ms_per_step": statistics.mean(secs) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": desc, "sample": sample},
+        "config": {"workload": desc, "sample": sample, "groups_per_step": 1,
+                   "groups_in_workload": len(groups_all), "flops_per_step": per_group},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -432,6 +508,7 @@ def run_ours(args):
     lse_ms = [e[4].elapsed_time(e[0]) for e in evs]
     tile_ms = [e[1].elapsed_time(e[2]) for e in evs]
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fin_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, device)
     flops = MET.counted_flops(p)
@@ -440,12 +517,6 @@ def run_ours(args):
 
     # roofline of the dominant kernel (the fused tile kernel)
     peaks, peak_src = load_peaks()
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
-    if p.dtype == W.DTYPE_BF16:
-        peak, peak_note = bf16_peak, f"bf16 dense, {peak_src} burst"
-    else:
-        peak = bf16_peak * TF32_OVER_BF16
-        peak_note = f"tf32 dense = {peak_src} bf16 burst x nominal 1.1/2.25"
     tile_mean = statistics.mean(tile_ms)
     achieved = flops / (tile_mean * 1e-3) / 1e12
     traffic = read_traffic(args.workload)
@@ -454,6 +525,8 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(p, x, dQ, dK, dV, ws, args, stream, world)
+    # after the timed regions: the reference products heat the GPU
+    peak, peak_note, peak_extra = tensor_peak(p, device, peaks, peak_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -480,7 +553,9 @@ def run_ours(args):
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": "dkdv_kernel (tcgen05 tile kernel)", "peak_source": peak_note,
                          "kernel_ms": tile_mean, "prep_ms": statistics.mean(prep_ms),
-                         "lse_ms": statistics.mean(lse_ms) if rec else 0.0},
+                         "finish_ms": statistics.mean(fin_ms),
+                         "lse_ms": statistics.mean(lse_ms) if rec else 0.0,
+                         "step_frac": value / peak, **peak_extra},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": ab.kernels_per_call(p, recompute_lse=rec) * args.steps,
@@ -543,11 +618,7 @@ def run_lse_only(args):
     flops = MET.lse_flops(p)
     value = whole_job_rate(flops, world, args.steps, total) / 1e12
     peaks, src = load_peaks()
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
-    if p.dtype == W.DTYPE_BF16:
-        peak, note = bf16_peak, f"bf16 dense, {src} burst"
-    else:
-        peak, note = bf16_peak * TF32_OVER_BF16, f"tf32 dense = {src} bf16 burst x nominal 1.1/2.25"
+    peak, note, peak_extra = tensor_peak(p, device, peaks, src)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import attention as OA
@@ -578,7 +649,8 @@ def run_lse_only(args):
                          "peak": peak, "unit": "TFLOP/s",
                          "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
                          "traffic": read_traffic(args.workload, prefix="lse_"),
-                         "kernel": "lse_kernel (persistent tcgen05)", "peak_source": note},
+                         "kernel": "lse_kernel (persistent tcgen05)", "peak_source": note,
+                         **peak_extra},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -640,11 +712,7 @@ def run_fwd(args):
     flops = 2.0 * MET.lse_flops(p)  # 2*D for S, 2*D for P V
     value = whole_job_rate(flops, world, args.steps, total) / 1e12
     peaks, src = load_peaks()
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
-    if p.dtype == W.DTYPE_BF16:
-        peak, note = bf16_peak, f"bf16 dense, {src} burst"
-    else:
-        peak, note = bf16_peak * TF32_OVER_BF16, f"tf32 dense = {src} bf16 burst x nominal 1.1/2.25"
+    peak, note, peak_extra = tensor_peak(p, device, peaks, src)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import attention as OA
@@ -676,7 +744,8 @@ def run_fwd(args):
                          "peak": peak, "unit": "TFLOP/s",
                          "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
                          "traffic": read_traffic(args.workload, prefix="fwd_"),
-                         "kernel": "fwd_kernel (persistent tcgen05)", "peak_source": note},
+                         "kernel": "fwd_kernel (persistent tcgen05)", "peak_source": note,
+                         **peak_extra},
             "cpu_baseline": cpu, "e2e": None,
             "gpu_launches": (1 if p.dtype == W.DTYPE_BF16 else 2) * args.steps,
             "clocks": clocks,
@@ -688,35 +757,93 @@ def run_fwd(args):
 
 
 def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
+    """The same metric end to end through the public API with host buffers.
+
+    Every step copies that step's inputs from pinned host memory to the
+    device, runs attn_bwd and copies dQ, dK, dV back to pinned host memory.
+    The three phases of consecutive steps overlap on three streams (inputs of
+    step k+1 and outputs of step k-1 move while step k computes), with two
+    device copies of the inputs and outputs so that a step never overwrites
+    what another step still reads.  Value = counted flops per step / mean
+    step time over the timed steps; the copy rates of each direction are
+    reported beside it."""
     import torch
     import attention_backward_pass_gb300 as ab
     names = (["Q", "K", "V", "O", "dO"] + ([] if args.recompute_lse else ["LSE"])
              + (["mask"] if x["mask"] is not None else []))
-    host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in names}
-    for k in names:
-        host[k].copy_(x[k])
-    dev = {k: torch.empty_like(x[k]) for k in names}
-    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (dQ, dK, dV)]
-    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
-    d2h = sum(t.numel() * t.element_size() for t in outs_h)
     n = max(3, min(args.steps, 10))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n + 2)]
-    for i in range(n + 2):  # first two untimed (warm-up)
-        evs[i][0].record(stream)
+    steps = n + 2  # the first two are untimed
+    host_in = [{k: torch.empty_like(x[k], device="cpu").pin_memory() for k in names}
+               for _ in range(2)]
+    for hb in host_in:
         for k in names:
-            dev[k].copy_(host[k], non_blocking=True)
-        ab.attn_bwd(p, dev["Q"], dev["K"], dev["V"], dev["O"], dev["dO"],
-                    None if args.recompute_lse else dev["LSE"], dev.get("mask"), dQ, dK, dV, ws)
-        for t_h, t_d in zip(outs_h, (dQ, dK, dV)):
-            t_h.copy_(t_d, non_blocking=True)
-        evs[i][1].record(stream)
+            hb[k].copy_(x[k])
+    dev_in = [{k: torch.empty_like(x[k]) for k in names} for _ in range(2)]
+    dev_out = [[torch.empty_like(t) for t in (dQ, dK, dV)] for _ in range(2)]
+    host_out = [[torch.empty_like(t, device="cpu").pin_memory() for t in (dQ, dK, dV)]
+                for _ in range(2)]
+    h2d = sum(host_in[0][k].numel() * host_in[0][k].element_size() for k in names)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    in_done = [ev() for _ in range(steps)]
+    comp_done = [ev() for _ in range(steps)]
+    out_done = [ev() for _ in range(steps)]
+    in_start = [ev() for _ in range(steps)]
+    out_start = [ev() for _ in range(steps)]
+    start = ev()
+
+    def issue_in(k):
+        s = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:  # the compute of step k-2 has read this input set
+                s_in.wait_event(comp_done[k - 2])
+            in_start[k].record(s_in)
+            for nm in names:
+                dev_in[s][nm].copy_(host_in[s][nm], non_blocking=True)
+            in_done[k].record(s_in)
+
     torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in evs[2:]) / n
+    start.record(stream)
+    issue_in(0)
+    for k in range(steps):
+        s = k % 2
+        if k + 1 < steps:
+            issue_in(k + 1)
+        stream.wait_event(in_done[k])
+        if k >= 2:  # step k-2's outputs have left this output set
+            stream.wait_event(out_done[k - 2])
+        d = dev_in[s]
+        ab.attn_bwd(p, d["Q"], d["K"], d["V"], d["O"], d["dO"],
+                    None if args.recompute_lse else d["LSE"], d.get("mask"), *dev_out[s], ws,
+                    stream=stream)
+        comp_done[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[k])
+            out_start[k].record(s_out)
+            for t_h, t_d in zip(host_out[s], dev_out[s]):
+                t_h.copy_(t_d, non_blocking=True)
+            out_done[k].record(s_out)
+    torch.cuda.synchronize()
+    if ab.check_device_error() != 0:
+        raise RuntimeError("device error word set during the end-to-end steps")
+    # step k ends when its outputs are on the host; timed: steps 2 .. steps-1
+    ms = out_done[1].elapsed_time(out_done[steps - 1]) / n
     ms = max_over_ranks(ms, dQ.device)
     value = MET.counted_flops(p) * world / (ms * 1e-3) / 1e12
+    h2d_ms = statistics.mean(in_start[k].elapsed_time(in_done[k]) for k in range(2, steps))
+    d2h_ms = statistics.mean(out_start[k].elapsed_time(out_done[k]) for k in range(2, steps))
+    # the last step's outputs match the device-resident run (dQ is summed in
+    # whatever order the key tiles finish, so only up to rounding)
+    for t_h, t_d in zip(host_out[(steps - 1) % 2], (dQ, dK, dV)):
+        a, b = t_h.to(t_d.device).float(), t_d.float()
+        if float((a - b).abs().max()) > 1e-5 * max(float(b.abs().max()), 1e-30):
+            raise RuntimeError("end-to-end outputs differ from the device-resident run")
     return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+            "pipelining": "H2D of step k+1 and D2H of step k-1 overlap step k (three streams, "
+                          "two buffer sets)"}
 
 
 def read_traffic(workload, prefix="dkdv_"):

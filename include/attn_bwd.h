@@ -271,8 +271,9 @@ attn_status attn_bwd_decode_kv(const attn_bwd_decode_params* p, const float* q,
  * fewer are used, so results can differ from attn_bwd_decode in the last bits.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current): make that first call before capturing
- * the stream into a CUDA graph.  All calls share the one array and nothing in
+ * device, with that device current, and again after the device's context
+ * has been replaced, e.g. by cudaDeviceReset): make that first call before
+ * capturing the stream into a CUDA graph.  All calls share the one array and nothing in
  * it is cleared between calls (each call rewrites every value it reads), so
  * calls that can overlap on the GPU -- on different streams or from different
  * host threads -- race; the caller must order them.
@@ -304,6 +305,9 @@ attn_status attn_bwd_query_range(const attn_bwd_params* p, int32_t k0, int32_t k
  * Synchronises nothing: reads (and, if clear_it, resets) the device error
  * word with a blocking copy on the current device.  Returns ATTN_OK or
  * ATTN_ERR_TIMEOUT.  Call after synchronising the streams that ran kernels.
+ * The word is a __device__ variable of the library; its address is looked up
+ * per device and again whenever the device's context has changed (after
+ * cudaDeviceReset the word starts at 0 in the new context).
  */
 attn_status attn_bwd_check_device_error(int32_t clear_it);
 

@@ -25,6 +25,34 @@ def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     return float(np.max(np.abs(gpu - ref))) / denom
 
 
+def strided_mask(p, kind, seed):
+    """Input synthesis for masked cases: a logical additive mask L [B, H, Sq, Sk] (N(0,1) values, 20 % at the
+    -1e30 sentinel, every head different) and the storage the oracle reads
+    through p's element strides:
+      per_head            [B, H, Sq, Sk]   strides (H Sq Sk, Sq Sk, Sk, 1)
+      per_head_transposed [B, H, Sk, Sq]   strides (H Sq Sk, Sq Sk, 1, Sq)
+      head_major          [H, B, Sk, Sq]   strides (Sq Sk, B Sq Sk, 1, Sq)
+    Sets the strides on p and returns (storage, L)."""
+    rng = np.random.default_rng(seed)
+    B, H, Sq, Sk = p.batch, p.num_heads, p.seq_q, p.seq_k
+    L = rng.standard_normal((B, H, Sq, Sk))
+    L[rng.random(L.shape) < 0.2] = W.MASKED
+    if kind == "per_head":
+        store = L.copy()
+        strides = (H * Sq * Sk, Sq * Sk, Sk, 1)
+    elif kind == "per_head_transposed":
+        store = np.ascontiguousarray(L.transpose(0, 1, 3, 2))
+        strides = (H * Sq * Sk, Sq * Sk, 1, Sq)
+    elif kind == "head_major":
+        store = np.ascontiguousarray(L.transpose(1, 0, 3, 2))
+        strides = (Sq * Sk, B * Sq * Sk, 1, Sq)
+    else:
+        raise ValueError(kind)
+    p.has_mask = 1
+    p.mask_stride_b, p.mask_stride_h, p.mask_stride_q, p.mask_stride_k = strides
+    return store, L
+
+
 def _torch_io(x, dtype, device):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)

@@ -13,7 +13,7 @@ from oracle import decode as OD
 from oracle import philox
 
 from parity_helpers import (TOL, compare, decode_case, make_case, rel_err, run_decode_gpu,
-                            run_decode_kv_gpu)
+                            run_decode_kv_gpu, strided_mask)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +41,17 @@ SMALL = {
                              dropout_prob=0.1, seed=0x5EED0004),
     "single_query_key": P(seq_q=1, seq_k=1),
     "empty_rows": P(seq_q=100, seq_k=90, window=5, causal_offset=80),
+    # mask + dropout on the D = 128 tile configurations
+    "mask_dropout_d128": P(seq_q=200, seq_k=333, head_dim=128, scale=1 / np.sqrt(128), causal=1,
+                           causal_offset=133, has_mask=1, dropout_prob=0.15, seed=0x5EED0006),
+    # GQA with mask + dropout, D = 64, [B,H,S,D]
+    "gqa_mask_dropout_d64_bhsd": P(num_heads=4, num_kv_heads=2, seq_q=190, seq_k=300, causal=1,
+                                   causal_offset=110, has_mask=1, dropout_prob=0.1,
+                                   seed=0x5EED0007),
+    "gqa_mask_dropout_d128_bshd": P(batch=2, num_heads=4, num_kv_heads=1, seq_q=150, seq_k=270,
+                                    head_dim=128, scale=1 / np.sqrt(128), causal=1,
+                                    causal_offset=120, has_mask=1, dropout_prob=0.2,
+                                    seed=0x5EED0008, layout=W.LAYOUT_BSHD),
 }
 
 
@@ -78,6 +89,52 @@ def test_real_valued_mask(kind, dtype):
     assert all(e <= TOL[dtype] for e in errs.values()), errs
 
 
+def _strided_mask_case(p, kind, seed):
+    """Seeded inputs with a per-(batch, query head) real-valued mask stored in
+    the layout ``kind`` (see parity_helpers.strided_mask); O and LSE from the
+    oracle forward."""
+    from oracle import attention as OA
+    Q, K, V, dO, _ = W.make_inputs(p, seed)
+    store, _ = strided_mask(p, kind, seed + 1)
+    store = store.astype(np.float32)
+    O, LSE = OA.forward(p, Q, K, V, store)
+    return dict(Q=Q, K=K, V=V, dO=dO, mask=store, O=W.round_io(O.astype(np.float32), p.dtype),
+                LSE=LSE.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("kind", ["per_head", "per_head_transposed", "head_major"])
+def test_strided_per_head_mask(kind, head_dim, dtype):
+    """A different mask for every (batch, query head) of a GQA problem, with
+    contiguous, transposed and head-major storage (mask strides b/h/q/k of
+    page 2's fab2_mask_at), plus dropout, on a ragged causal shape."""
+    p = P(batch=2, num_heads=4, num_kv_heads=2, seq_q=150, seq_k=270, head_dim=head_dim,
+          scale=1 / np.sqrt(head_dim), causal=1, causal_offset=120, dropout_prob=0.1,
+          seed=0x5EED000A, layout=W.LAYOUT_BSHD)
+    p.dtype = dtype
+    case = _strided_mask_case(p, kind, seed=606)
+    errs = compare(p, case)
+    assert all(e <= TOL[dtype] for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("recompute_lse", [False, True], ids=["lse_given", "lse_recomputed"])
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_everything_mix(head_dim, dtype, recompute_lse):
+    """Every rule of page 2 at once: GQA (3 query heads per KV head), causal
+    with an offset, a sliding window, a real-valued per-head additive mask
+    with sentinels, dropout, [B,S,H,D], on a shape with ragged query and key
+    tails."""
+    p = P(batch=2, num_heads=6, num_kv_heads=2, seq_q=211, seq_k=345, head_dim=head_dim,
+          scale=1 / np.sqrt(head_dim), causal=1, causal_offset=134, window=150,
+          dropout_prob=0.2, seed=0x5EED000B, layout=W.LAYOUT_BSHD)
+    p.dtype = dtype
+    case = _strided_mask_case(p, "per_head", seed=707)
+    errs = compare(p, case, recompute_lse=recompute_lse)
+    assert all(e <= TOL[dtype] for e in errs.values()), errs
+
+
 def test_keep_mask_bit_exact():
     import torch
     import attention_backward_pass_gb300 as ab
@@ -101,8 +158,8 @@ def test_repeat_calls_overwrite():
 FULL = {
     "tiny": (W.tiny, None),
     "causal_mha": (W.causal_mha, [(0, 0), (3, 15), (2, 6)]),
-    "gqa_window_f32": (lambda: W.gqa_window(W.DTYPE_F32), [(0, 0), (1, 7)]),
-    "gqa_window_bf16": (lambda: W.gqa_window(W.DTYPE_BF16), [(1, 3)]),
+    "gqa_window_f32": (lambda: W.gqa_window(W.DTYPE_F32), [(0, 0), (0, 5), (1, 7)]),
+    "gqa_window_bf16": (lambda: W.gqa_window(W.DTYPE_BF16), [(0, 0), (1, 3), (1, 7)]),
     "masked_dropout": (W.masked_dropout, [(0, 0), (1, 9)]),
 }
 

@@ -21,6 +21,8 @@ from oracle import attention as A
 from oracle import decode as Dec
 from oracle import philox
 
+from parity_helpers import strided_mask
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -131,34 +133,6 @@ def test_against_torch_autograd(name):
     np.testing.assert_allclose(LSE, lse_t, rtol=1e-12, atol=1e-12)
     for a, b in ((dQ, dq_t), (dK, dk_t), (dV, dv_t)):
         np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
-
-
-def strided_mask(p, kind, seed):
-    """A logical additive mask L [B, H, Sq, Sk] (N(0,1) values, 20 % at the
-    -1e30 sentinel, every head different) and the storage the oracle reads
-    through p's element strides:
-      per_head            [B, H, Sq, Sk]   strides (H Sq Sk, Sq Sk, Sk, 1)
-      per_head_transposed [B, H, Sk, Sq]   strides (H Sq Sk, Sq Sk, 1, Sq)
-      head_major          [H, B, Sk, Sq]   strides (Sq Sk, B Sq Sk, 1, Sq)
-    Sets the strides on p and returns (storage, L)."""
-    rng = np.random.default_rng(seed)
-    B, H, Sq, Sk = p.batch, p.num_heads, p.seq_q, p.seq_k
-    L = rng.standard_normal((B, H, Sq, Sk))
-    L[rng.random(L.shape) < 0.2] = W.MASKED
-    if kind == "per_head":
-        store = L.copy()
-        strides = (H * Sq * Sk, Sq * Sk, Sk, 1)
-    elif kind == "per_head_transposed":
-        store = np.ascontiguousarray(L.transpose(0, 1, 3, 2))
-        strides = (H * Sq * Sk, Sq * Sk, 1, Sq)
-    elif kind == "head_major":
-        store = np.ascontiguousarray(L.transpose(1, 0, 3, 2))
-        strides = (Sq * Sk, B * Sq * Sk, 1, Sq)
-    else:
-        raise ValueError(kind)
-    p.has_mask = 1
-    p.mask_stride_b, p.mask_stride_h, p.mask_stride_q, p.mask_stride_k = strides
-    return store, L
 
 
 @pytest.mark.parametrize("kind", ["per_head", "per_head_transposed", "head_major"])

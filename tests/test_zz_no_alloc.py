@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 
 
-def _run_both(p, seed):
+def _run_both(p, seed, oracle_seqs=()):
     import torch
     import attention_backward_pass_gb300 as ab
     case = decode_case(p, seed)
@@ -46,12 +46,32 @@ def _run_both(p, seed):
         assert np.all(np.isfinite(s)) and np.all(np.isfinite(q))
         assert rel_err(s, ref_s) <= TOL, rel_err(s, ref_s)
         assert rel_err(q, ref_q) <= TOL, rel_err(q, ref_q)
+        if oracle_seqs:
+            from oracle import decode as OD
+            seqs = list(oracle_seqs)
+            rds, rdq = OD.decode_backward(case["k"], case["v"], case["probs"], case["d_out"],
+                                          seqs=seqs)
+            assert rel_err(s[seqs], rds[seqs]) <= TOL, rel_err(s[seqs], rds[seqs])
+            assert rel_err(q[seqs], rdq[seqs]) <= TOL, rel_err(q[seqs], rdq[seqs])
 
 
 @pytest.mark.parametrize("prob", [W.decode(), W.DecodeProblem(3, 4, 2, 64, 17)],
                          ids=["64seq_8h_d256_4096", "3seq_4h_2kv_d64_17"])
 def test_noalloc_matches_workspace_entry_point(prob):
     _run_both(prob, seed=11)
+
+
+def test_noalloc_uses_fewer_splits_when_the_usual_ones_do_not_fit():
+    """900 (sequence, KV head) pairs with D = 256, 8 query heads per KV head
+    and a 64-key history: the partial sums of the usual split count (one
+    split per SM, each holding a slot for every pair it touches) need more
+    than the 8 MiB array, those of one split fit, so the entry point runs
+    with fewer splits.  Checked against the workspace entry point and, on a
+    few sequences, against the fp64 oracle."""
+    import attention_backward_pass_gb300 as ab
+    p = W.DecodeProblem(900, 8, 1, 256, 64)
+    assert ab.decode_workspace_size(p) > (8 << 20)
+    _run_both(p, seed=13, oracle_seqs=(0, 450, 899))
 
 
 def test_noalloc_rejects_problem_beyond_scratch():
