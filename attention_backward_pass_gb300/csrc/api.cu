@@ -455,6 +455,7 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
   a.det = p->deterministic;
   a.dK = dK;
   a.dV = dV;
+  a.V = V;
   a.n_kv_tiles = (p->seq_k + bn - 1) / bn;
   a.err = err;
   if (launch_dkdv(*p, maps, a, stream) != cudaSuccess) return ATTN_ERR_CUDA;

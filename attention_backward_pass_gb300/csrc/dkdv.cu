@@ -70,26 +70,46 @@ struct Cfg;
 // tile t's own natural Q / dO stage (GEMM1/2 are done with it by then), which
 // is released to the producer only after GEMM5; VTM: V lives in tensor memory
 // as GEMM2's A operand, so GEMM2 reads only the dO tile from shared memory.
+//
+// The fp32 D = 128 configuration adds four options (all false elsewhere):
+// SPLITQ: Q and dO travel in rings of their own (NAT Q slots, NDO dO slots);
+//   a dO slot is released as soon as GEMM2 has read it, a Q slot holds the
+//   tile's dS' after GEMM1 and is released after GEMM5.
+// VGL: V goes from global memory straight into tensor memory (softmax warps,
+//   rounded to TF32), without a shared-memory staging copy.
+// DQA: the dQ^T accumulator of tile t lives in the P columns of score buffer
+//   t % NSB: GEMM5 (t) is issued once GEMM3/4 (t) are complete, and GEMM1/2
+//   (t + NSB) wait until the dQ warps have drained it.
+// DQRED: the dQ warps add dQ into global memory with fp32 reductions straight
+//   from registers (no shared-memory staging tile).
+// FRAG: the unmasked fp32 softmax uses 16x256b fragments (BM = 64 only).
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
-  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 1, NSB = 2, PB = 1;
+  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 3;
   static constexpr bool KMAJ = true, DQT = true, INPL = true, VTM = true;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
-  static constexpr int BN = 64, BM = 32, NAT = 2, TR = 1, NSB = 2, PB = 1;
-  static constexpr bool KMAJ = true, DQT = true, INPL = false, VTM = false;
+  static constexpr int BN = 128, BM = 32, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 1;
+  static constexpr bool KMAJ = true, DQT = true, INPL = true, VTM = true;
+  static constexpr bool SPLITQ = true, VGL = true, DQA = true, DQRED = true, FRAG = false;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
-  static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1;
+  static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
   static constexpr bool KMAJ = false, DQT = false, INPL = false, VTM = false;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
-  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1;
+  static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
   static constexpr bool KMAJ = false, DQT = true, INPL = false, VTM = false;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
 };
+
+// the dQ^T accumulator [M5 lanes][N5 columns] fits in the BM P columns
+constexpr bool L_N5_FITS(int n5, int bm) { return n5 <= bm; }
 
 template <bool BF16, int D>
 struct Layout {
@@ -97,6 +117,9 @@ struct Layout {
   static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB,
                        PB = C::PB;
   static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT, INPL = C::INPL, VTM = C::VTM;
+  static constexpr bool SPLITQ = C::SPLITQ, VGL = C::VGL, DQA = C::DQA, DQRED = C::DQRED,
+                        FRAG = C::FRAG;
+  static constexpr int NDO = SPLITQ ? C::NDO : NAT;  // dO slots (= NAT unless SPLITQ)
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
   static constexpr int W = 128 / E;       // elements per 128-byte segment
   static constexpr int KSTEP = 32 / E;    // K elements per MMA instruction
@@ -109,11 +132,14 @@ struct Layout {
   static constexpr int OFF_V = OFF_K + K_BYTES;  // must follow K (padded GEMM5 reads it)
   static constexpr int OFF_KT = OFF_V + (VTM ? 0 : K_BYTES);
   // natural ring [NAT]: separate Q and dO rings, or (INPL) stages of
-  // [Q tile][dO tile] that later hold the tile's dS' [BM rows][BN keys]
+  // [Q tile][dO tile] that later hold the tile's dS' [BM rows][BN keys], or
+  // (SPLITQ) NAT Q slots (later dS') and NDO dO slots
   static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);
-  static constexpr int NAT_STRIDE = INPL ? 2 * Q_BYTES : Q_BYTES;
-  static constexpr int OFF_DO = OFF_Q + (INPL ? Q_BYTES : NAT * Q_BYTES);
-  static constexpr int OFF_QT = OFF_Q + 2 * NAT * Q_BYTES;     // transposed ring [TR]
+  static constexpr bool JOINT = INPL && !SPLITQ;  // [Q | dO] stages
+  static constexpr int NAT_STRIDE = JOINT ? 2 * Q_BYTES : Q_BYTES;
+  static constexpr int OFF_DO = OFF_Q + (JOINT ? Q_BYTES : NAT * Q_BYTES);
+  static constexpr int OFF_QT =
+      SPLITQ ? OFF_DO + NDO * Q_BYTES : OFF_Q + 2 * NAT * Q_BYTES;  // transposed ring [TR]
   static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
   // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
   static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
@@ -125,7 +151,7 @@ struct Layout {
   static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
-  static constexpr int STG_D = DQT ? (D > 64 ? 64 : D) : 0;
+  static constexpr int STG_D = (DQT && !DQRED) ? (D > 64 ? 64 : D) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
   // (fp32, D=64) dropout keep bits of two query tiles, [2][BN keys][BM / 16]
   // x 16 bits, drawn by the dQ warps one tile ahead of the softmax warps; the
@@ -134,14 +160,15 @@ struct Layout {
   static constexpr int NCH = BM / 16;
   static constexpr int OFF_BITS = OFF_STG + BM * STG_D * 4;
   static constexpr int OFF_BAR = OFF_BITS + (DBITS ? 2 * BN * NCH * 2 : 0);
-  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9;
+  static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9 +
+                                  2 * NDO + NSB;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
-  static constexpr int NAT_TX = 2 * Q_BYTES;
+  static constexpr int NAT_TX = SPLITQ ? Q_BYTES : 2 * Q_BYTES;
   static constexpr int TR_TX = 2 * Q_BYTES;
   static constexpr int ROW_TX = 2 * BM * 4;
-  static constexpr int KV_TX = (KMAJ ? 3 : 2) * K_BYTES;
+  static constexpr int KV_TX = ((KMAJ ? 3 : 2) - (VGL ? 1 : 0)) * K_BYTES;
   // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
   static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
   static constexpr int N5 = DQT ? BM : D;
@@ -152,7 +179,7 @@ struct Layout {
   static constexpr int T_DS = T_P + (INPL ? 0 : PB * PCOLS);
   static constexpr int T_DV = T_DS + (KMAJ && !INPL ? PB * BM : 0), T_DK = T_DV + D,
                        T_DQ = T_DK + D;
-  static constexpr int T_V = T_DQ + N5;
+  static constexpr int T_V = T_DQ + (DQA ? 0 : N5);
   static constexpr int T_USED = T_V + (VTM ? D : 0);
   static constexpr int T_ALLOC = T_USED <= 256 ? 256 : 512;
   // softmax split: two warps per TMEM sub-partition, each on half the columns
@@ -166,8 +193,13 @@ struct Layout {
   static_assert(BN == 64 || BN == 128, "key tile");
   static_assert(!INPL || (KMAJ && !BF16 && NAT_STRIDE >= P_BYTES && NAT >= 3),
                 "in-place P / dS' is the fp32 layout; dS' fits a natural stage");
-  static_assert(!VTM || (INPL && BN == 128 && 2 * TR * Q_BYTES >= K_BYTES && D / W == 2),
+  static_assert(!VTM || (INPL && BN == 128 && (VGL || (2 * TR * Q_BYTES >= K_BYTES && D / W == 2))),
                 "V staging through the transposed ring, one column block per softmax half");
+  static_assert(!SPLITQ || (INPL && NDO >= 1), "split rings hold dS' in the Q slot");
+  static_assert(!DQA || (INPL && NSB == 2 && KMAJ && BF16 == false && L_N5_FITS(N5, BM)),
+                "dQ^T aliases the P columns of its score buffer");
+  static_assert(!DQRED || (DQT && KMAJ && M5 == 128 && N5 == BM), "register dQ reduction");
+  static_assert(!FRAG || (INPL && BM == 64 && D == 64), "16x256b softmax fragments");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
 
@@ -434,6 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_ready = kv_full + 5;           // (VTM) V copied into tensor memory
   uint64_t* pfree = kv_full + 6;             // [NSB] (INPL) GEMM3/4 done with buffer b
   uint64_t* bits_full = pfree + NSB;         // [2] dropout keep bits of a tile drawn (by parity)
+  uint64_t* do_full = bits_full + 2;         // [NDO] (SPLITQ) dO tile landed
+  uint64_t* do_empty = do_full + L::NDO;     // [NDO] (SPLITQ) GEMM2 done with the dO slot
+  uint64_t* dq_free_b = do_empty + L::NDO;   // [NSB] (DQA) dQ^T of buffer b drained
   uint16_t* bits_s = reinterpret_cast<uint16_t*>(smem + L::OFF_BITS);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
   constexpr int RST = L::ROW_ST;
@@ -472,6 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NSB; ++s) mbar_init(&pfree[s], 1);
     mbar_init(&bits_full[0], kDqThreads);
     mbar_init(&bits_full[1], kDqThreads);
+    for (int s = 0; s < L::NDO; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
+    }
+    for (int s = 0; s < NSB; ++s) mbar_init(&dq_free_b[s], kDqThreads);
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -494,8 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(kv_full, L::KV_TX);
       for (int cb = 0; cb < L::NB_D; ++cb) {
         tma_load_4d(smem + L::OFF_K + cb * BN * 128, &tm_k, kv_full, cb * W, w.k0, w.kvh, w.b);
-        tma_load_4d(smem + L::OFF_VLOAD + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh,
-                    w.b);
+        if constexpr (!L::VGL)
+          tma_load_4d(smem + L::OFF_VLOAD + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh,
+                      w.b);
       }
       if constexpr (L::KMAJ) {
         // K^T [D rows][BN keys]: one box of W keys x D rows per column block
@@ -503,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + L::OFF_KT + cb * D * 128, &tm_kt, kv_full, w.k0 + cb * W, 0, bhkv,
                       0);
       }
-      int nat_issued = 0, row_issued = 0;
+      int nat_issued = 0, row_issued = 0, do_issued = 0;
       for (int t = 0; t < T; ++t) {
         const int g = t / w.tiles_per_head;
         const int h = w.kvh * a.group + g;
@@ -517,11 +558,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < L::NB_D; ++cb) {
           tma_load_4d(smem + L::OFF_Q + s * L::NAT_STRIDE + cb * BM * 128, &tm_q, &nat_full[s],
                       cb * W, q0, h, w.b);
-          tma_load_4d(smem + L::OFF_DO + s * L::NAT_STRIDE + cb * BM * 128, &tm_do,
-                      &nat_full[s],
-                      cb * W, q0, h, w.b);
+          if constexpr (!L::SPLITQ)
+            tma_load_4d(smem + L::OFF_DO + s * L::NAT_STRIDE + cb * BM * 128, &tm_do,
+                        &nat_full[s], cb * W, q0, h, w.b);
         }
         nat_issued = t + 1;
+        if constexpr (L::SPLITQ) {
+          // dO slot of its own, released by GEMM2
+          const int so = t % L::NDO;
+          if (t >= L::NDO && !mbar_wait(&do_empty[so], ((t / L::NDO) - 1) & 1, a.err)) break;
+          mbar_expect_tx(&do_full[so], L::Q_BYTES);
+          for (int cb = 0; cb < L::NB_D; ++cb)
+            tma_load_4d(smem + L::OFF_DO + so * L::Q_BYTES + cb * BM * 128, &tm_do, &do_full[so],
+                        cb * W, q0, h, w.b);
+          do_issued = t + 1;
+        }
         // LSE2 / Delta rows of the tile: a ring of their own, released by the
         // softmax warps as soon as they finish the tile
         const int rr = t % RST;
@@ -535,6 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(kv_full, 0);
       for (int t = (nat_issued > NAT ? nat_issued - NAT : 0); t < nat_issued; ++t)
         drain_wait(&nat_full[t % NAT], (t / NAT) & 1);
+      for (int t = (do_issued > L::NDO ? do_issued - L::NDO : 0); t < do_issued; ++t)
+        drain_wait(&do_full[t % L::NDO], (t / L::NDO) & 1);
       for (int t = (row_issued > RST ? row_issued - RST : 0); t < row_issued; ++t)
         drain_wait(&row_full[t % RST], (t / RST) & 1);
     }
@@ -550,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tr_issued = 0;
         // VTM: the first transposed tiles overwrite the staged V, so they wait
         // until the softmax warps have moved it into tensor memory
-        const bool v_ok = !L::VTM || mbar_wait(v_ready, 0, a.err);
+        const bool v_ok = !L::VTM || L::VGL || mbar_wait(v_ready, 0, a.err);
         for (int t = 0; v_ok && t < T; ++t) {
           const int g = t / w.tiles_per_head;
           const int h = w.kvh * a.group + g;
@@ -601,15 +654,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
       bool ok = mbar_wait(kv_full, 0, a.err);
       auto issue_front = [&](int t) -> bool {  // GEMM1, GEMM2 of tile t
-        const int s = t % NAT, b = t % NSB;
+        const int s = t % NAT, b = t % NSB, so = t % L::NDO;
         if (!mbar_wait(&nat_full[s], (t / NAT) & 1, a.err)) return false;
+        if (L::SPLITQ && !mbar_wait(&do_full[so], (t / L::NDO) & 1, a.err)) return false;
         // buffer b is free once the softmax warps have read its scores, or
-        // (in place) once GEMM3/4 have read the P / dS' written over them
+        // (in place) once GEMM3/4 have read the P / dS' written over them,
+        // and (DQA) once the dQ warps have drained the dQ^T held there
         if (t >= NSB &&
             !mbar_wait(L::INPL ? &pfree[b] : &s_free[b], ((t / NSB) - 1) & 1, a.err))
           return false;
+        if (L::DQA && t >= NSB && !mbar_wait(&dq_free_b[b], ((t / NSB) - 1) & 1, a.err))
+          return false;
         tc_fence_after();
-        const uint64_t dQ = adv(dQ0, s * L::NAT_STRIDE), dDO = adv(dDO0, s * L::NAT_STRIDE);
+        const uint64_t dQ = adv(dQ0, s * L::NAT_STRIDE);
+        const uint64_t dDO = adv(dDO0, L::SPLITQ ? so * L::Q_BYTES : s * L::NAT_STRIDE);
         const uint32_t t_s = tmem + b * 2 * BM, t_dp = t_s + BM;
 #pragma unroll
         for (int ks = 0; ks < D / L::KSTEP; ++ks) {
@@ -626,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full[b]);
         // natural tiles done with (INPL: the stage then holds dS' until GEMM5)
         if constexpr (L::KMAJ && !L::INPL) mma_commit(&nat_empty[s]);
+        if constexpr (L::SPLITQ) mma_commit(&do_empty[so]);
         return true;
       };
       auto issue_back34 = [&](int t) -> bool {  // GEMM3, GEMM4 of tile t
@@ -665,9 +724,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_g5 = [&](int t) -> bool {  // GEMM5 of tile t
-        const int s = t % NAT, pb = t % PB;
-        if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
+        const int s = t % NAT, pb = t % PB, b = t % NSB;
+        if constexpr (L::DQA) {
+          // GEMM5 writes dQ^T over the P columns of buffer b: GEMM3/4 (t),
+          // which read them, must be complete.  The dQ warps must also have
+          // taken tile t - 1's accumulator (already true when GEMM1/2 (t + 1)
+          // were issued), so that mma5_done never runs two phases ahead of them
+          if (!mbar_wait(&pfree[b], (t / NSB) & 1, a.err)) return false;
+          if (t > 0 && !mbar_wait(&dq_free_b[(t - 1) % NSB], ((t - 1) / NSB) & 1, a.err))
+            return false;
+        } else {
+          if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
+        }
         tc_fence_after();
+        const uint32_t t_dq = L::DQA ? tmem + (uint32_t)(b * 2 * BM) : tmem + L::T_DQ;
 #pragma unroll
         for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
           if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T, both K-major over keys
@@ -675,13 +745,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ka = (kb / 128) * D * 128 + (kb % 128);
             const uint32_t na = (L::INPL ? s * L::NAT_STRIDE : pb * L::P_BYTES) +
                                 (kb / 128) * BM * 128 + (kb % 128);
-            mma_ss<BF16>(tmem + L::T_DQ, adv(dKT, ka), adv(dSN, na), id_dq, ks > 0);
+            mma_ss<BF16>(t_dq, adv(dKT, ka), adv(dSN, na), id_dq, ks > 0);
           } else if constexpr (L::DQT) {
             const uint32_t ra = ks * L::KSTEP * 128;
-            mma_ss<BF16>(tmem + L::T_DQ, adv(mK, ra), adv(mS, ra), id_dq, ks > 0);
+            mma_ss<BF16>(t_dq, adv(mK, ra), adv(mS, ra), id_dq, ks > 0);
           } else {
             const uint32_t ra = ks * L::KSTEP * 128;
-            mma_ss<BF16>(tmem + L::T_DQ, adv(mS, ra), adv(mK, ra), id_dq, ks > 0);
+            mma_ss<BF16>(t_dq, adv(mS, ra), adv(mK, ra), id_dq, ks > 0);
           }
         }
         mma_commit(mma5_done);
@@ -700,10 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && mbar_wait(v_ready, 0, a.err);
         tc_fence_after();
       }
-      for (int t = 0; ok && t < NSB && t < T; ++t)
+      // DQA: GEMM1/2 run one tile ahead (a buffer is busy until its dQ^T is
+      // drained): front (t + 1) is issued before waiting for the softmax of
+      // tile t, so the softmax of t + 1 overlaps GEMM3/4 (t) and GEMM5 (t);
+      // front (t + 1) itself waits for the dQ warps to take dQ^T (t - 1)
+      constexpr int NPRE = L::DQA ? 1 : NSB;
+      for (int t = 0; ok && t < NPRE && t < T; ++t)
         if (!issue_front(t)) ok = false;
       for (int t = 0; ok && t < T; ++t) {
-        if constexpr (L::INPL) {
+        if constexpr (L::DQA) {
+          ok = (t + 1 >= T || issue_front(t + 1)) && issue_back34(t) && issue_g5(t);
+        } else if constexpr (L::INPL) {
           ok = issue_back34(t) && issue_g5(t) && (t + NSB >= T || issue_front(t + NSB));
         } else {
           ok = (t + NSB >= T || issue_front(t + NSB)) && issue_back34(t) && issue_g5(t);
@@ -743,7 +820,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 2; ++e) xo2[2 * k + e] = (uint32_t)((((tr / 4 + 2 * k) ^ (2 * tq + e))) << 4);
     bool ok = true;
-    if constexpr (L::VTM) {
+    if constexpr (L::VTM && L::VGL) {
+      if (T > 0) {
+        // V into tensor memory (GEMM2's A operand) straight from global
+        // memory: this lane's key row, this warp's half of the head dimension,
+        // rounded to TF32 like the tiles TMA delivers; keys past the end of
+        // the sequence are zero
+        constexpr int DH = D / 2;
+        const float* vrow = reinterpret_cast<const float*>(a.V) +
+                            row_offset(a.layout, w.b, w.kvh, key_ok ? kj : 0, a.Hkv, a.Sk, D) +
+                            half * DH;
+#pragma unroll 1
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t rv[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 v4 = key_ok ? __ldg(reinterpret_cast<const float4*>(vrow + c0) + c)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            rv[4 * c] = to_tf32(v4.x);
+            rv[4 * c + 1] = to_tf32(v4.y);
+            rv[4 * c + 2] = to_tf32(v4.z);
+            rv[4 * c + 3] = to_tf32(v4.w);
+          }
+          __syncwarp();  // tcgen05.st is warp-collective
+          tmem_st16(tmem + lane_base + L::T_V + half * DH + c0, rv);
+        }
+        tmem_st_wait();
+        // releases tensor memory's V to the MMA issuer
+        tc_fence_before();
+        mbar_arrive(v_ready);
+      }
+    } else if constexpr (L::VTM) {
       if (T > 0) {
         // V into tensor memory (GEMM2's A operand): this lane's key row, this
         // warp's column block of the swizzled tile, 32 fp32 = 32 columns
@@ -801,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint16_t* kbits = bits_s + ((t & 1) * BN + jj) * L::NCH;
-      if (L::INPL && !a.has_mask && !a.dropout) {
+      if (L::FRAG && !a.has_mask && !a.dropout) {
         softmax_frag(a, t_s + cbeg, t_dp + cbeg, sLSE + cbeg, sDelta + cbeg, plain, q0 + cbeg,
                      w.k0 + quad * 32, key_ok4, dsn_base + dsn_frag, xo2);
       } else {
@@ -1084,23 +1191,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!dq_group_all(mbar_wait(mma5_done, t & 1, a.err))) break;
       tc_fence_after();
       __syncwarp();  // tcgen05.ld is warp-collective; the staging below diverges on r
+      // (DQA) the accumulator of tile t sits in the P columns of its buffer
+      const uint32_t t_dq =
+          L::DQA ? (uint32_t)((t % NSB) * 2 * BM) : (uint32_t)L::T_DQ;
       float v[L::N5];
 #pragma unroll
       for (int c0 = 0; c0 < L::N5; c0 += 16) {
         uint32_t rr[16];
-        tmem_ld16(tmem + lane_base + L::T_DQ + c0, rr);
+        tmem_ld16(tmem + lane_base + t_dq + c0, rr);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c) v[c0 + c] = __uint_as_float(rr[c]);
       }
       tc_fence_before();
-      mbar_arrive(dq_free);
+      mbar_arrive(L::DQA ? &dq_free_b[t % NSB] : dq_free);
       const int nq = min(BM, a.Sq - q0);
       // deterministic: this key tile's own dQ slice, [kt * B + b][h][q][d]
       const int kt = w.k0 / BN;
       float* gbase = a.det ? a.dq_acc + row_offset(0, kt * a.B + w.b, h, q0, a.H, a.Sq, D)
                            : a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
-      if constexpr (L::DQT) {
+      if constexpr (L::DQRED) {
+        // lane r holds head-dim column r of dQ^T for the tile's BM queries:
+        // fp32 reductions (deterministic mode: stores into this key tile's
+        // slice), coalesced along d across the warp
+        if (r >= 0) {
+          const long long qstride = a.det ? D : rstride;
+          float* dst = gbase + r;
+#pragma unroll
+          for (int c = 0; c < BM; ++c) {  // v[] stays in registers: constant indices
+            if (c < nq) {
+              if (a.det)
+                dst[c * qstride] = v[c];
+              else
+                atomicAdd(dst + c * qstride, v[c]);
+            }
+          }
+        }
+      } else if constexpr (L::DQT) {
         // stage [BM queries][STG d] and hand the tile to the TMA engine as one
         // reduce-add (rows past Sq fall outside the tensor map and are skipped)
         constexpr int STG = L::STG_D;

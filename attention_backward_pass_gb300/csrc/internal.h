@@ -38,6 +38,7 @@ struct TileArgs {
   int det;             // 1: store dQ slices instead of adding into dq_acc
   void* dK;
   void* dV;
+  const void* V;       // V itself (configurations that load it into tensor memory directly)
   int n_kv_tiles;
   unsigned int* err;
 };
