@@ -834,10 +834,12 @@ def run_e2e(p, x, dQ, dK, dV, ws, args, stream, world):
     h2d_ms = statistics.mean(in_start[k].elapsed_time(in_done[k]) for k in range(2, steps))
     d2h_ms = statistics.mean(out_start[k].elapsed_time(out_done[k]) for k in range(2, steps))
     # the last step's outputs match the device-resident run (dQ is summed in
-    # whatever order the key tiles finish, so only up to rounding)
+    # whatever order the key tiles finish, so only up to rounding: fp32
+    # rounding, or one bf16 unit after the bf16 conversion)
+    tol = 1e-2 if p.dtype == W.DTYPE_BF16 else 1e-5
     for t_h, t_d in zip(host_out[(steps - 1) % 2], (dQ, dK, dV)):
         a, b = t_h.to(t_d.device).float(), t_d.float()
-        if float((a - b).abs().max()) > 1e-5 * max(float(b.abs().max()), 1e-30):
+        if float((a - b).abs().max()) > tol * max(float(b.abs().max()), 1e-30):
             raise RuntimeError("end-to-end outputs differ from the device-resident run")
     return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
