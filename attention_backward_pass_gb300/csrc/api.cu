@@ -562,6 +562,8 @@ attn_status attn_fwd(const attn_bwd_params* p, const void* Q, const void* K, con
   a.msq = p->mask_stride_q;
   a.msk = p->mask_stride_k;
   a.mask = mask;
+  a.mask_vec = p->has_mask && aligned16(mask) && a.msk == 1 && a.msq % 4 == 0 &&
+               a.msh % 4 == 0 && a.msb % 4 == 0;
   a.dropout = p->dropout_prob > 0.f ? 1 : 0;
   a.drop_threshold = dropout_threshold(p->dropout_prob);
   a.drop_inv_keep = (float)(1.0 / (1.0 - (double)p->dropout_prob));

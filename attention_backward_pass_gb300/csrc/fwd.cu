@@ -375,9 +375,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < QC; ++e) mv[e] = 0.f;
         if (mrow && kb < hi && kb + QC > lo) {
+          if (a.mask_vec) {
+            // contiguous, 16-byte aligned mask rows (kb is a multiple of 16)
 #pragma unroll
-          for (int e = 0; e < QC; ++e)
-            if (kb + e < a.Sk) mv[e] = __ldg(mrow + (long long)(kb + e) * a.msk);
+            for (int e = 0; e < QC; e += 4) {
+              if (kb + e + 4 <= a.Sk) {
+                const float4 v4 = __ldg(reinterpret_cast<const float4*>(mrow + kb + e));
+                mv[e] = v4.x;
+                mv[e + 1] = v4.y;
+                mv[e + 2] = v4.z;
+                mv[e + 3] = v4.w;
+              } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (kb + e + u < a.Sk) mv[e + u] = __ldg(mrow + kb + e + u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < QC; ++e)
+              if (kb + e < a.Sk) mv[e] = __ldg(mrow + (long long)(kb + e) * a.msk);
+          }
         }
         uint32_t sv[QC];
 #pragma unroll
@@ -445,20 +463,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st_wait();
           }
         }
-        // dropout keep bits of the share (bit e: key kb + e), one Philox4x32-10
-        // call per key with counter (q >> 2, key, b * H + h, 0), word q & 3
+        // dropout keep bits of the share (bit e: key kb + e) from Philox4x32-10
+        // with counter (q >> 2, key, b * H + h, 0), word q & 3.  The four rows
+        // of one q >> 2 are lanes 4m .. 4m + 3 of the warp (the item starts at a
+        // multiple of 128 rows), so each call serves all four: for keys
+        // 4j .. 4j + 3 lane 4m + i computes key 4j + i, and a 4 x 4 transpose by
+        // XOR shuffles hands every lane its own word of the four keys
         uint32_t keep = 0xFFFFFFFFu;
         if (a.dropout) {
           keep = 0u;
+          const int li = lane & 3;
 #pragma unroll 1
-          for (int e = 0; e < QC; ++e) {
-            const Philox4 rnd = philox4x32_10((uint32_t)q >> 2, (uint32_t)(kb + e), bh32, 0u,
-                                              a.seed_lo, a.seed_hi);
-            const uint32_t word = (q & 3) == 0   ? rnd.w[0]
-                                  : (q & 3) == 1 ? rnd.w[1]
-                                  : (q & 3) == 2 ? rnd.w[2]
-                                                 : rnd.w[3];
-            keep |= (word >= a.drop_threshold ? 1u : 0u) << e;
+          for (int j = 0; j < QC; j += 4) {
+            const Philox4 rnd = philox4x32_10((uint32_t)q >> 2, (uint32_t)(kb + j + li), bh32,
+                                              0u, a.seed_lo, a.seed_hi);
+            // word w of this lane's key belongs to query (q & ~3) + w = lane (lane & ~3) | w
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int w = li ^ m;  // the word the partner lane needs
+              const uint32_t send = w == 0 ? rnd.w[0] : w == 1 ? rnd.w[1] : w == 2 ? rnd.w[2] : rnd.w[3];
+              // from partner li ^ m: its key j + (li ^ m), our word li
+              const uint32_t word = m == 0 ? send : __shfl_xor_sync(0xffffffffu, send, m);
+              keep |= (word >= a.drop_threshold ? 1u : 0u) << (j + (li ^ m));
+            }
           }
         }
         const float mul = a.dropout ? a.drop_inv_keep : 1.f;

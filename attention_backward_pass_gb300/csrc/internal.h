@@ -145,7 +145,7 @@ struct FwdArgs {
   float scale_log2e;  // scale * log2(e)
   int causal;
   long long causal_offset, window;
-  int has_mask;
+  int has_mask, mask_vec;  // mask_vec: rows are contiguous and 16-byte aligned
   long long msb, msh, msq, msk;
   const float* mask;
   int dropout;              // 0 / 1
