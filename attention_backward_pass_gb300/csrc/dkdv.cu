@@ -161,7 +161,7 @@ struct Layout {
   static constexpr int OFF_BITS = OFF_STG + BM * STG_D * 4;
   static constexpr int OFF_BAR = OFF_BITS + (DBITS ? 2 * BN * NCH * 2 : 0);
   static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9 +
-                                  2 * NDO + NSB;
+                                  2 * NDO + 2 * NSB;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   // bytes landing per stage and for the resident key tiles
@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bits_full = pfree + NSB;         // [2] dropout keep bits of a tile drawn (by parity)
   uint64_t* do_full = bits_full + 2;         // [NDO] (SPLITQ) dO tile landed
   uint64_t* do_empty = do_full + L::NDO;     // [NDO] (SPLITQ) GEMM2 done with the dO slot
-  uint64_t* dq_free_b = do_empty + L::NDO;   // [NSB] (DQA) dQ^T of buffer b drained
+  uint64_t* dq_free_b = do_empty + L::NDO;   // [NSB] (DQA) GEMM3 has read P of buffer b
+  uint64_t* dq_drained = dq_free_b + NSB;    // [NSB] (DQA) dQ^T of buffer b drained
   uint16_t* bits_s = reinterpret_cast<uint16_t*>(smem + L::OFF_BITS);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMPTR);
   constexpr int RST = L::ROW_ST;
@@ -511,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&do_full[s], 1);
       mbar_init(&do_empty[s], 1);
     }
-    for (int s = 0; s < NSB; ++s) mbar_init(&dq_free_b[s], kDqThreads);
+    for (int s = 0; s < NSB; ++s) mbar_init(&dq_free_b[s], 1);
+    for (int s = 0; s < NSB; ++s) mbar_init(&dq_drained[s], kDqThreads);
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -663,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= NSB &&
             !mbar_wait(L::INPL ? &pfree[b] : &s_free[b], ((t / NSB) - 1) & 1, a.err))
           return false;
-        if (L::DQA && t >= NSB && !mbar_wait(&dq_free_b[b], ((t / NSB) - 1) & 1, a.err))
+        if (L::DQA && t >= NSB && !mbar_wait(&dq_drained[b], ((t / NSB) - 1) & 1, a.err))
           return false;
         tc_fence_after();
         const uint64_t dQ = adv(dQ0, s * L::NAT_STRIDE);
@@ -705,6 +707,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           bdo0 = adv(mDO0, s * L::NAT_STRIDE);
           bq0 = adv(mQ0, s * L::NAT_STRIDE);
         }
+        if constexpr (L::DQA) {
+          // GEMM3 (reads P) first, then GEMM4: GEMM5, which overwrites the P
+          // columns, only waits for GEMM3
+#pragma unroll
+          for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
+            const uint32_t kb = ks * 32;
+            const uint32_t ba = (kb / 128) * D * 128 + (kb % 128);
+            mma_ts<BF16>(tmem + L::T_DV, t_p + ks * 8, adv(bdo0, ba), id_acc, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&dq_free_b[b]);  // (DQA) P of buffer b read
+#pragma unroll
+          for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
+            const uint32_t kb = ks * 32;
+            const uint32_t ba = (kb / 128) * D * 128 + (kb % 128);
+            mma_ts<BF16>(tmem + L::T_DK, t_ds + ks * 8, adv(bq0, ba), id_acc, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+        } else {
 #pragma unroll
         for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
           const uint32_t kb = ks * 32;
@@ -719,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss<BF16>(tmem + L::T_DK, adv(dS, pa), adv(bq0, ba), id_acc, acc);
           }
         }
+        }
         if constexpr (L::INPL) mma_commit(&pfree[b]);  // score buffer b reusable
         if constexpr (L::KMAJ) mma_commit(&tr_empty[r]);  // GEMM5 does not read them
         return true;
@@ -730,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // which read them, must be complete.  The dQ warps must also have
           // taken tile t - 1's accumulator (already true when GEMM1/2 (t + 1)
           // were issued), so that mma5_done never runs two phases ahead of them
-          if (!mbar_wait(&pfree[b], (t / NSB) & 1, a.err)) return false;
-          if (t > 0 && !mbar_wait(&dq_free_b[(t - 1) % NSB], ((t - 1) / NSB) & 1, a.err))
+          if (!mbar_wait(&dq_free_b[b], (t / NSB) & 1, a.err)) return false;  // GEMM3 (t) done
+          if (t > 0 && !mbar_wait(&dq_drained[(t - 1) % NSB], ((t - 1) / NSB) & 1, a.err))
             return false;
         } else {
           if (t > 0 && !mbar_wait(dq_free, (t - 1) & 1, a.err)) return false;
@@ -1204,7 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 16; ++c) v[c0 + c] = __uint_as_float(rr[c]);
       }
       tc_fence_before();
-      mbar_arrive(L::DQA ? &dq_free_b[t % NSB] : dq_free);
+      mbar_arrive(L::DQA ? &dq_drained[t % NSB] : dq_free);
       const int nq = min(BM, a.Sq - q0);
       // deterministic: this key tile's own dQ slice, [kt * B + b][h][q][d]
       const int kt = w.k0 / BN;
