@@ -173,7 +173,7 @@ def _wsb(workspace):
 
 
 def attn_bwd_prepare(p, Q, K, O, dO, LSE, dQ, workspace, stream=None):
-    """Stage 1 of attn_bwd: Delta, LSE*log2(e), dQ accumulator reset, transposes."""
+    """Stage 1 of attn_bwd: Delta, LSE*log2(e), dQ accumulator reset."""
     st = load_library().attn_bwd_prepare(ctypes.byref(make_params(p)), _ptr(Q), _ptr(K), _ptr(O),
                                          _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(workspace),
                                          _wsb(workspace), _stream_ptr(stream))

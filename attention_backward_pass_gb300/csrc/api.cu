@@ -77,12 +77,10 @@ attn_status validate(const attn_bwd_params* p) {
 // Workspace carve-up (each region 256-byte aligned):
 //   delta, lse2   [B*H][sq_pad] fp32
 //   dq_acc        fp32 dQ accumulator (bf16 only; fp32 accumulates in dQ)
-//   qt, dot, kt   transposed fp32 copies [B*H][D][sq_pad], [B*Hkv][D][sk_pad]
-//                 (fp32 only: TF32 products take K-major operands)
 //   dqp           deterministic dQ: one fp32 slice per key tile,
 //                 [n_kv_tiles * B][H][Sq][D]
 struct WsLayout {
-  size_t delta, lse2, dq_acc, qt, dot, kt, dqp, total;
+  size_t delta, lse2, dq_acc, dqp, total;
   int sq_pad, sk_pad;
 };
 
@@ -96,13 +94,7 @@ WsLayout ws_layout(const attn_bwd_params& p) {
   w.lse2 = align256(rows * 4);
   w.dq_acc = w.lse2 + align256(rows * 4);
   const size_t dq = bf ? align256((size_t)p.batch * p.num_heads * p.seq_q * p.head_dim * 4) : 0;
-  w.qt = w.dq_acc + dq;
-  const size_t qt = bf ? 0 : align256(rows * p.head_dim * 4);
-  w.dot = w.qt + qt;
-  w.kt = w.dot + qt;
-  const size_t kt =
-      bf ? 0 : align256((size_t)p.batch * p.num_kv_heads * w.sk_pad * p.head_dim * 4);
-  w.dqp = w.kt + kt;
+  w.dqp = w.dq_acc + dq;
   size_t dqp = 0;
   if (p.deterministic) {
     const size_t n_kt = (size_t)((p.seq_k + dkdv_block_n(p.dtype, p.head_dim) - 1) /
@@ -111,21 +103,6 @@ WsLayout ws_layout(const attn_bwd_params& p) {
   }
   w.total = w.dqp + dqp;
   return w;
-}
-
-// Transposed fp32 copy [BH][D][s_pad]; the map's extent along s is the true
-// length, so TMA fills the padding columns with zeros.
-CUresult make_map_t(CUtensorMap* m, const void* base, int D, int S, int s_pad, int BH) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
-  cuuint64_t dims[4] = {(cuuint64_t)S, (cuuint64_t)D, (cuuint64_t)BH, 1};
-  cuuint64_t strides[3] = {(cuuint64_t)s_pad * 4, (cuuint64_t)s_pad * D * 4,
-                           (cuuint64_t)s_pad * D * 4 * BH};
-  cuuint32_t box[4] = {32, (cuuint32_t)D, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_TFLOAT32, 4, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // fp32 dQ accumulator in the problem's layout, unswizzled boxes of
@@ -152,8 +129,11 @@ CUresult make_map_dq(CUtensorMap* m, void* base, int D, int S, int H, int B, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Natural [.., S, .., D] tensor in boxes of 128 bytes x box_rows, 128-byte
+// swizzle (K-major operand tiles); atom32 (fp32 only): the 128-byte swizzle of
+// 32-byte atoms, the layout of a TF32 operand read MN-major.
 CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int H, int B,
-                  int layout, int box_rows) {
+                  int layout, int box_rows, bool atom32 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
   const int e = dtype == ATTN_BF16 ? 2 : 4;
@@ -173,8 +153,8 @@ CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int
   // fp32 tensors are fetched as TF32 (the operand type of the products)
   return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_TFLOAT32,
              4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+             atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 }  // namespace
@@ -267,7 +247,7 @@ namespace {
 
 struct Plan {
   WsLayout wl;
-  float *delta, *lse2, *dq_acc, *qt, *dot, *kt, *dqp;
+  float *delta, *lse2, *dq_acc, *dqp;
 };
 
 attn_status make_plan(const attn_bwd_params* p, void* dQ, void* workspace, size_t workspace_bytes,
@@ -284,9 +264,6 @@ attn_status make_plan(const attn_bwd_params* p, void* dQ, void* workspace, size_
   pl->lse2 = reinterpret_cast<float*>(ws + pl->wl.lse2);
   pl->dq_acc = p->dtype == ATTN_BF16 ? reinterpret_cast<float*>(ws + pl->wl.dq_acc)
                                      : reinterpret_cast<float*>(dQ);
-  pl->qt = reinterpret_cast<float*>(ws + pl->wl.qt);
-  pl->dot = reinterpret_cast<float*>(ws + pl->wl.dot);
-  pl->kt = reinterpret_cast<float*>(ws + pl->wl.kt);
   pl->dqp = reinterpret_cast<float*>(ws + pl->wl.dqp);
   return ATTN_OK;
 }
@@ -350,15 +327,8 @@ attn_status prepare_impl(const attn_bwd_params* p, const void* Q, const void* K,
   if (st != ATTN_OK) return st;
   if (!all_aligned({Q, K, O, dO})) return ATTN_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
-  cudaError_t e;
-  if (p->dtype == ATTN_BF16) {
-    e = launch_prep(*p, O, dO, LSE, pl.delta, pl.lse2, pl.wl.sq_pad, pl.dq_acc, stream);
-  } else {
-    e = launch_prep_f32(*p, static_cast<const float*>(Q), static_cast<const float*>(K),
-                        static_cast<const float*>(O), static_cast<const float*>(dO), LSE, pl.delta,
-                        pl.lse2, pl.dq_acc, pl.qt, pl.dot, pl.kt, pl.wl.sq_pad, pl.wl.sk_pad,
-                        stream);
-  }
+  const cudaError_t e =
+      launch_prep(*p, O, dO, LSE, pl.delta, pl.lse2, pl.wl.sq_pad, pl.dq_acc, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -398,13 +368,15 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
   memset(&maps, 0, sizeof(maps));
   const int bm = dkdv_block_m(p->dtype, p->head_dim);
   const int bn = dkdv_block_n(p->dtype, p->head_dim);
+  // fp32: the MN-major copies of Q, dO and K (GEMM3/4/5) come from the same
+  // tensors, fetched with the 128-byte swizzle of 32-byte atoms
   if (p->dtype != ATTN_BF16 &&
-      (make_map_t(&maps.qt, pl.qt, p->head_dim, p->seq_q, pl.wl.sq_pad,
-                  p->batch * p->num_heads) != CUDA_SUCCESS ||
-       make_map_t(&maps.dot, pl.dot, p->head_dim, p->seq_q, pl.wl.sq_pad,
-                  p->batch * p->num_heads) != CUDA_SUCCESS ||
-       make_map_t(&maps.kt, pl.kt, p->head_dim, p->seq_k, pl.wl.sk_pad,
-                  p->batch * p->num_kv_heads) != CUDA_SUCCESS))
+      (make_map(&maps.qt, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
+                bm, true) != CUDA_SUCCESS ||
+       make_map(&maps.dot, dO, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch,
+                p->layout, bm, true) != CUDA_SUCCESS ||
+       make_map(&maps.kt, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch,
+                p->layout, bn, true) != CUDA_SUCCESS))
     return ATTN_ERR_CUDA;
   if (make_map(&maps.q, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
                bm) != CUDA_SUCCESS ||
@@ -505,9 +477,7 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
 
 size_t attn_fwd_workspace_size(const attn_bwd_params* p) {
   if (validate(p) != ATTN_OK) return 0;
-  if (p->dtype == ATTN_BF16) return 256;  // not used
-  return align256((size_t)p->batch * p->num_kv_heads * round_up(p->seq_k, kRowPad) *
-                  p->head_dim * 4);
+  return 256;  // not used: the forward needs no scratch
 }
 
 attn_status attn_fwd(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
@@ -524,26 +494,16 @@ attn_status attn_fwd(const attn_bwd_params* p, const void* Q, const void* K, con
   unsigned int* err = device_error_word();
   if (!err) return ATTN_ERR_CUDA;
   const int bn = fwd_block_n(p->dtype, p->head_dim);
-  const int sk_pad = round_up(p->seq_k, kRowPad);
   CUtensorMap tq, tk, tv;
   if (make_map(&tq, Q, p->dtype, p->head_dim, p->seq_q, p->num_heads, p->batch, p->layout,
                128) != CUDA_SUCCESS ||
       make_map(&tk, K, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
                bn) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  if (p->dtype == ATTN_BF16) {
-    if (make_map(&tv, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
-                 bn) != CUDA_SUCCESS)
-      return ATTN_ERR_CUDA;
-  } else {
-    // fp32: V^T [B*Hkv][D][sk_pad], TF32-rounded, in the workspace
-    float* vt = reinterpret_cast<float*>(workspace);
-    if (launch_transpose_kv_f32(*p, static_cast<const float*>(V), vt, sk_pad, stream) !=
-            cudaSuccess ||
-        make_map_t(&tv, vt, p->head_dim, p->seq_k, sk_pad, p->batch * p->num_kv_heads) !=
-            CUDA_SUCCESS)
-      return ATTN_ERR_CUDA;
-  }
+  // V is read MN-major by O += P . V (fp32: in the 32-byte-atom swizzle)
+  if (make_map(&tv, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout, bn,
+               p->dtype != ATTN_BF16) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
   FwdArgs a;
   memset(&a, 0, sizeof(a));
   a.B = p->batch;

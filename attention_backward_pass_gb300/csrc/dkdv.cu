@@ -18,13 +18,15 @@
 // exactly what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B.
 //  * bf16: one copy of each tile serves as a K-major operand (rows = M/N) and
 //    as an MN-major operand (rows = K).
-//  * fp32 (TF32 products): the tensor cores take TF32 operands K-major only,
-//    so the contractions over queries (GEMM3/4) and keys (GEMM5) read
-//    transposed copies Q^T, dO^T, K^T that the prepare stage writes to the
-//    workspace, and the softmax warps also write dS' in [query][key]
-//    orientation.  The natural tiles (GEMM1/2) and the transposed tiles
-//    (GEMM3/4) travel in separate rings, so a natural stage is released as
-//    soon as GEMM1/2 are done with it.
+//  * fp32 (TF32 products): a TF32 operand read MN-major must be laid out in
+//    the 128-byte swizzle of 32-byte atoms ([MN / 32][K rows][128 bytes],
+//    32-byte chunk index XOR (row & 3)), which differs from the K-major
+//    tiles' swizzle.  So the contractions over queries (GEMM3/4) and keys
+//    (GEMM5) read second copies of the Q, dO and K tiles that TMA loads from
+//    the same tensors with that swizzle (the "MN-major copies"), and the
+//    softmax warps write dS' in [query][key] orientation.  The natural tiles
+//    (GEMM1/2) and the MN-major copies (GEMM3/4) travel in separate rings, so
+//    a natural stage is released as soon as GEMM1/2 are done with it.
 //
 // Pipeline.  GEMM1/2 of tile t + NSB are issued as soon as score buffer
 // t % NSB is free (NSB = 1 or 2 score buffers), then GEMM3-5 of tile t once
@@ -43,7 +45,7 @@
 //   warp 0       TMA producer: resident key tiles, natural Q / dO ring
 //   warp 1       MMA issuer (one elected lane)
 //   warp 2       TMEM allocator
-//   warp 3       TMA producer of the transposed ring (fp32)
+//   warp 3       TMA producer of the MN-major Q / dO copies (fp32)
 //   warps 4-11   softmax: warp w serves TMEM sub-partition w % 4 (its key
 //                rows) and half (w - 4) / 4 of the query columns; turns S^T
 //                and dP^T into P o M and dS', stores them as MMA operands, and
@@ -139,15 +141,15 @@ struct Layout {
   static constexpr int NAT_STRIDE = JOINT ? 2 * Q_BYTES : Q_BYTES;
   static constexpr int OFF_DO = OFF_Q + (JOINT ? Q_BYTES : NAT * Q_BYTES);
   static constexpr int OFF_QT =
-      SPLITQ ? OFF_DO + NDO * Q_BYTES : OFF_Q + 2 * NAT * Q_BYTES;  // transposed ring [TR]
+      SPLITQ ? OFF_DO + NDO * Q_BYTES : OFF_Q + 2 * NAT * Q_BYTES;  // MN-major copy ring [TR]
   static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
   // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
   static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
   static constexpr int OFF_DSN = OFF_DS + (KMAJ ? 0 : P_BYTES);
   static constexpr int ROW_ST = 4;  // stages of the LSE2 / Delta ring
   static constexpr int OFF_LSE = OFF_DSN + (KMAJ && !INPL ? PB * P_BYTES : 0);
-  // VTM: V lands in the (not yet used) transposed ring and is moved into
-  // tensor memory before the first transposed tiles are fetched
+  // VTM: V lands in the (not yet used) MN-major copy ring and is moved into
+  // tensor memory before the first MN-major copies are fetched
   static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
@@ -187,14 +189,14 @@ struct Layout {
   static_assert(T_USED <= 512 && TR_TX > 0, "tensor memory budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(COLS % 16 == 0, "softmax column chunks");
-  static_assert(!KMAJ || (BM % W == 0 && TR >= 1), "transposed tiles are whole blocks");
+  static_assert(!KMAJ || (D % W == 0 && BM % KSTEP == 0 && TR >= 1), "MN-major copies");
   static_assert(KMAJ || NAT >= 2, "stages are released only after GEMM3/4");
   static_assert(PB == 1 || PB == 2, "P / dS buffers");
   static_assert(BN == 64 || BN == 128, "key tile");
   static_assert(!INPL || (KMAJ && !BF16 && NAT_STRIDE >= P_BYTES && NAT >= 3),
                 "in-place P / dS' is the fp32 layout; dS' fits a natural stage");
   static_assert(!VTM || (INPL && BN == 128 && (VGL || (2 * TR * Q_BYTES >= K_BYTES && D / W == 2))),
-                "V staging through the transposed ring, one column block per softmax half");
+                "V staging through the MN-major copy ring, one column block per softmax half");
   static_assert(!SPLITQ || (INPL && NDO >= 1), "split rings hold dS' in the Q slot");
   static_assert(!DQA || (INPL && NSB == 2 && KMAJ && BF16 == false && L_N5_FITS(N5, BM)),
                 "dQ^T aliases the P columns of its score buffer");
@@ -450,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* nat_full = bars;                 // [NAT] natural tiles landed (TMA tx)
   uint64_t* nat_empty = nat_full + NAT;      // [NAT] natural stage free (MMA commit)
-  uint64_t* tr_full = nat_empty + NAT;       // [TR] transposed tiles + LSE2/Delta landed
-  uint64_t* tr_empty = tr_full + TR;         // [TR] transposed stage free (MMA commit)
+  uint64_t* tr_full = nat_empty + NAT;       // [TR] MN-major Q / dO copies landed
+  uint64_t* tr_empty = tr_full + TR;         // [TR] MN-major copy stage free (MMA commit)
   uint64_t* row_full = tr_empty + TR;        // [ROW_ST] LSE2 / Delta of a tile landed
   uint64_t* row_empty = row_full + L::ROW_ST;  // [ROW_ST] softmax warps done with them
   uint64_t* s_full = row_empty + L::ROW_ST;  // [NSB] GEMM1/2 done into score buffer b
@@ -532,7 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      const int bhkv = w.b * a.Hkv + w.kvh;
       mbar_expect_tx(kv_full, L::KV_TX);
       for (int cb = 0; cb < L::NB_D; ++cb) {
         tma_load_4d(smem + L::OFF_K + cb * BN * 128, &tm_k, kv_full, cb * W, w.k0, w.kvh, w.b);
@@ -541,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       w.b);
       }
       if constexpr (L::KMAJ) {
-        // K^T [D rows][BN keys]: one box of W keys x D rows per column block
-        for (int cb = 0; cb < BN / W; ++cb)
-          tma_load_4d(smem + L::OFF_KT + cb * D * 128, &tm_kt, kv_full, w.k0 + cb * W, 0, bhkv,
-                      0);
+        // MN-major copy of K for GEMM5: [D / W blocks][BN keys][W columns]
+        for (int cb = 0; cb < L::NB_D; ++cb)
+          tma_load_4d(smem + L::OFF_KT + cb * BN * 128, &tm_kt, kv_full, cb * W, w.k0, w.kvh,
+                      w.b);
       }
       int nat_issued = 0, row_issued = 0, do_issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -595,30 +596,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();  // reconverge before the block-wide barrier at the end
   } else if (warp == 3) {
-    // ------------------------------------------------- transposed-tile producer
-    // (fp32) Q^T / dO^T tiles [D rows][BM] and LSE2 / Delta, in a ring of its
-    // own so it never holds up the natural tiles that GEMM1/2 wait for
+    // ------------------------------------------------- MN-major copy producer
+    // (fp32) the tile's Q and dO again, [D / W blocks][BM rows][W columns] in
+    // the 32-byte-atom swizzle, in a ring of its own so it never holds up the
+    // natural tiles that GEMM1/2 wait for
     if constexpr (L::KMAJ) {
       if (elect_one_sync() && T > 0) {
         tma_prefetch_desc(&tm_qt);
         tma_prefetch_desc(&tm_dot);
         int tr_issued = 0;
-        // VTM: the first transposed tiles overwrite the staged V, so they wait
+        // VTM: the first MN-major copies overwrite the staged V, so they wait
         // until the softmax warps have moved it into tensor memory
         const bool v_ok = !L::VTM || L::VGL || mbar_wait(v_ready, 0, a.err);
         for (int t = 0; v_ok && t < T; ++t) {
           const int g = t / w.tiles_per_head;
           const int h = w.kvh * a.group + g;
-          const int bh = w.b * a.H + h;
           const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
           const int r = t % TR;
           if (t >= TR && !mbar_wait(&tr_empty[r], ((t / TR) - 1) & 1, a.err)) break;
           mbar_expect_tx(&tr_full[r], L::TR_TX);
-          for (int cb = 0; cb < BM / W; ++cb) {
-            tma_load_4d(smem + L::OFF_QT + r * L::Q_BYTES + cb * D * 128, &tm_qt, &tr_full[r],
-                        q0 + cb * W, 0, bh, 0);
-            tma_load_4d(smem + L::OFF_DOT + r * L::Q_BYTES + cb * D * 128, &tm_dot, &tr_full[r],
-                        q0 + cb * W, 0, bh, 0);
+          for (int cb = 0; cb < L::NB_D; ++cb) {
+            tma_load_4d(smem + L::OFF_QT + r * L::Q_BYTES + cb * BM * 128, &tm_qt, &tr_full[r],
+                        cb * W, q0, h, w.b);
+            tma_load_4d(smem + L::OFF_DOT + r * L::Q_BYTES + cb * BM * 128, &tm_dot, &tr_full[r],
+                        cb * W, q0, h, w.b);
           }
           tr_issued = t + 1;
         }
@@ -634,20 +635,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // addresses stay below 256 KB, so the add never carries out of the field.
     if (elect_one_sync() && T > 0) {
       constexpr uint32_t id_s = make_idesc(BF16, BN, BM, false, false);
-      constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, !L::KMAJ);
-      constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, !L::KMAJ, !L::KMAJ);
+      // GEMM3/4 read dO / Q MN-major; GEMM5 reads K MN-major (and, bf16, dS')
+      constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, true);
+      constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, true, !L::KMAJ);
       // K-major tiles: LBO unused, SBO = 8 rows x 128 B
       const uint64_t dK = sw128_desc(smem_u32(smem + L::OFF_K), 16, 1024);
       const uint64_t dV = sw128_desc(smem_u32(smem + L::OFF_V), 16, 1024);
       const uint64_t dS = sw128_desc(smem_u32(smem + L::OFF_DS), 16, 1024);
-      const uint64_t dKT = sw128_desc(smem_u32(smem + L::OFF_KT), 16, 1024);
       // fp32 dS' [BM rows][BN keys]: its own region, or (INPL) natural stage 0
       const uint64_t dSN =
           sw128_desc(smem_u32(smem + (L::INPL ? L::OFF_Q : L::OFF_DSN)), 16, 1024);
       const uint64_t dQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), 16, 1024);
       const uint64_t dDO0 = sw128_desc(smem_u32(smem + L::OFF_DO), 16, 1024);
-      const uint64_t dQT0 = sw128_desc(smem_u32(smem + L::OFF_QT), 16, 1024);
-      const uint64_t dDOT0 = sw128_desc(smem_u32(smem + L::OFF_DOT), 16, 1024);
+      // (fp32) MN-major copies in the 32-byte-atom swizzle: K [D / W][BN][W],
+      // Q and dO [D / W][BM][W]
+      const uint64_t aKT = mn32_desc(smem_u32(smem + L::OFF_KT), BN * 128);
+      const uint64_t aQT0 = mn32_desc(smem_u32(smem + L::OFF_QT), BM * 128);
+      const uint64_t aDOT0 = mn32_desc(smem_u32(smem + L::OFF_DOT), BM * 128);
       // MN-major views (bf16): LBO = bytes between 128-byte column blocks
       const uint64_t mQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), BM * 128, 1024);
       const uint64_t mDO0 = sw128_desc(smem_u32(smem + L::OFF_DO), BM * 128, 1024);
@@ -700,9 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint64_t bdo0, bq0;
-        if constexpr (L::KMAJ) {  // transposed tiles [D rows][BM], K-major
-          bdo0 = adv(dDOT0, r * L::Q_BYTES);
-          bq0 = adv(dQT0, r * L::Q_BYTES);
+        if constexpr (L::KMAJ) {  // MN-major copies of the tile's dO / Q
+          bdo0 = adv(aDOT0, r * L::Q_BYTES);
+          bq0 = adv(aQT0, r * L::Q_BYTES);
         } else {  // natural tiles [BM rows][D] read MN-major
           bdo0 = adv(mDO0, s * L::NAT_STRIDE);
           bq0 = adv(mQ0, s * L::NAT_STRIDE);
@@ -712,15 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // columns, only waits for GEMM3
 #pragma unroll
           for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
-            const uint32_t kb = ks * 32;
-            const uint32_t ba = (kb / 128) * D * 128 + (kb % 128);
+            const uint32_t ba = ks * L::KSTEP * 128;  // K step = KSTEP rows
             mma_ts<BF16>(tmem + L::T_DV, t_p + ks * 8, adv(bdo0, ba), id_acc, (t > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(&dq_free_b[b]);  // (DQA) P of buffer b read
 #pragma unroll
           for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
-            const uint32_t kb = ks * 32;
-            const uint32_t ba = (kb / 128) * D * 128 + (kb % 128);
+            const uint32_t ba = ks * L::KSTEP * 128;
             mma_ts<BF16>(tmem + L::T_DK, t_ds + ks * 8, adv(bq0, ba), id_acc, (t > 0 || ks > 0) ? 1u : 0u);
           }
         } else {
@@ -728,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < BM / L::KSTEP; ++ks) {
           const uint32_t kb = ks * 32;
           const uint32_t pa = (kb / 128) * BN * 128 + (kb % 128);
-          const uint32_t ba = L::KMAJ ? (kb / 128) * D * 128 + (kb % 128) : ks * L::KSTEP * 128;
+          const uint32_t ba = ks * L::KSTEP * 128;  // MN-major: K step = KSTEP rows
           const uint32_t acc = (t > 0 || ks > 0) ? 1u : 0u;
           // 8 TMEM columns hold one K step (8 tf32, or 16 bf16 packed in pairs)
           mma_ts<BF16>(tmem + L::T_DV, t_p + ks * 8, adv(bdo0, ba), id_acc, acc);
@@ -760,12 +762,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_dq = L::DQA ? tmem + (uint32_t)(b * 2 * BM) : tmem + L::T_DQ;
 #pragma unroll
         for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
-          if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T, both K-major over keys
+          if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T: K MN-major, dS' K-major
             const uint32_t kb = ks * 32;
-            const uint32_t ka = (kb / 128) * D * 128 + (kb % 128);
+            const uint32_t ka = ks * L::KSTEP * 128;
             const uint32_t na = (L::INPL ? s * L::NAT_STRIDE : pb * L::P_BYTES) +
                                 (kb / 128) * BM * 128 + (kb % 128);
-            mma_ss<BF16>(t_dq, adv(dKT, ka), adv(dSN, na), id_dq, ks > 0);
+            mma_ss<BF16>(t_dq, adv(aKT, ka), adv(dSN, na), id_dq, ks > 0);
           } else if constexpr (L::DQT) {
             const uint32_t ra = ks * L::KSTEP * 128;
             mma_ss<BF16>(t_dq, adv(mK, ra), adv(mS, ra), id_dq, ks > 0);
@@ -894,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
         }
-        // releases the staged V to the transposed-tile producer and tensor
+        // releases the staged V to the MN-major copy producer and tensor
         // memory's V to the MMA issuer
         tc_fence_before();
         mbar_arrive(v_ready);

@@ -26,9 +26,9 @@
 //   warp 3      idle
 //   warps 4-19  softmax / correction / epilogue
 // Operands: Q and K K-major (128-byte swizzle) for S; for O += P . V the A
-// operand is P in TMEM and the B operand is V: the natural [keys][D] tile read
-// MN-major for bf16, the transposed copy V^T [D][keys] (TF32-rounded, from the
-// workspace) read K-major for fp32, whose tensor-core operands must be K-major.
+// operand is P in TMEM and the B operand is the natural [keys][D] tile of V
+// read MN-major: 128-byte swizzle for bf16; for fp32 the 128-byte swizzle of
+// 32-byte atoms, the layout TF32 operands read MN-major take.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -246,17 +246,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             break;
           }
           mbar_expect_tx(&v_full[sv], L::V_BYTES);
-          if constexpr (BF16) {
-            // natural V [BN keys][D]: column blocks of W elements
-            for (int cb = 0; cb < L::NB_D; ++cb)
-              tma_load_4d(smem + L::OFF_V + sv * L::V_BYTES + cb * BN * 128, &tm_v, &v_full[sv],
-                          cb * W, k0, kvh, it.b);
-          } else {
-            // V^T [D rows][BN keys]: one box of W keys x D rows per column block
-            for (int cb = 0; cb < BN / W; ++cb)
-              tma_load_4d(smem + L::OFF_V + sv * L::V_BYTES + cb * D * 128, &tm_v, &v_full[sv],
-                          k0 + cb * W, 0, it.b * (a.H / a.group) + kvh, 0);
-          }
+          // natural V [BN keys][D]: column blocks of W elements
+          for (int cb = 0; cb < L::NB_D; ++cb)
+            tma_load_4d(smem + L::OFF_V + sv * L::V_BYTES + cb * BN * 128, &tm_v, &v_full[sv],
+                        cb * W, k0, kvh, it.b);
           ++gv;
         }
       }
@@ -269,12 +262,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       constexpr uint32_t id_s = make_idesc(BF16, BM, BN, false, false);
-      // O += P . V: A = P in TMEM; B = V read MN-major (bf16) or V^T K-major (fp32)
-      constexpr uint32_t id_o = make_idesc(BF16, BM, D, false, BF16);
+      // O += P . V: A = P in TMEM; B = V read MN-major
+      constexpr uint32_t id_o = make_idesc(BF16, BM, D, false, true);
       const uint64_t dQ0 = sw128_desc(smem_u32(smem + L::OFF_Q), 16, 1024);
       const uint64_t dK0 = sw128_desc(smem_u32(smem + L::OFF_K), 16, 1024);
       const uint64_t dV0 = BF16 ? sw128_desc(smem_u32(smem + L::OFF_V), BN * 128, 1024)
-                                : sw128_desc(smem_u32(smem + L::OFF_V), 16, 1024);
+                                : mn32_desc(smem_u32(smem + L::OFF_V), BN * 128);
       auto adv = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (uint64_t)(bytes >> 4); };
       int g = 0, gs = 0, nz = 0;  // tiles whose P . V was issued, S issued, items
       bool ok = true;
@@ -318,8 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
             // 8 TMEM columns hold one K step of P (8 tf32, or 16 bf16 in pairs)
-            const uint32_t va = BF16 ? ks * L::KSTEP * 128
-                                     : ((ks * 32) / 128) * D * 128 + ((ks * 32) % 128);
+            const uint32_t va = ks * L::KSTEP * 128;  // K step = KSTEP rows
             mma_ts<BF16>(tmem + L::T_O, tmem + L::T_S + sb * BN + ks * 8, adv(dV, va), id_o,
                          (t > 0 || ks > 0) ? 1u : 0u);
           }

@@ -95,7 +95,7 @@ cudaError_t launch_dq_reduce(const attn_bwd_params& p, const float* slices, void
 
 struct TileMaps {
   CUtensorMap q, k, v, dout;  // natural [.., S, .., D] tensors
-  CUtensorMap qt, kt, dot;    // transposed copies [B*H][D][S_pad] (fp32 path)
+  CUtensorMap qt, kt, dot;    // fp32: Q, K, dO again, 32-byte-atom swizzle (MN-major reads)
   CUtensorMap dq;             // fp32 dQ accumulator (reduce-add target)
 };
 cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,
@@ -104,11 +104,6 @@ int dkdv_block_m(int dtype, int head_dim);
 int dkdv_block_n(int dtype, int head_dim);
 int dkdv_dq_box_d(int dtype, int head_dim);  // head-dim columns per dQ reduce box
 
-// fp32 prepare in one pass: Delta, -LSE*log2(e), zeroed dQ, Q^T, dO^T, K^T.
-cudaError_t launch_prep_f32(const attn_bwd_params& p, const float* Q, const float* K,
-                            const float* O, const float* dO, const float* LSE, float* delta,
-                            float* nlse, float* dq, float* qt, float* dot, float* kt, int sq_pad,
-                            int sk_pad, cudaStream_t stream);
 
 uint32_t dropout_threshold(float prob);
 cudaError_t launch_dropout_mask(const attn_bwd_params& p, int b, int h, uint8_t* keep,
@@ -156,15 +151,11 @@ struct FwdArgs {
   float* LSE;  // [B*H][Sq]
   unsigned int* err;
 };
-// tq: Q, boxes of 128 rows; tk: K, boxes of fwd_block_n rows; tv: V (bf16,
-// boxes of fwd_block_n rows) or V^T [B*Hkv][D][sk_pad] (fp32, boxes of 32 keys
-// x D rows).
+// tq: Q, boxes of 128 rows; tk: K and tv: V, boxes of fwd_block_n rows (fp32
+// V in the 128-byte swizzle of 32-byte atoms, read MN-major).
 int fwd_block_n(int dtype, int head_dim);
 cudaError_t launch_fwd(const attn_bwd_params& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream);
-// fp32 V^T [B*Hkv][D][sk_pad], TF32-rounded (the key side of the fp32 prepare).
-cudaError_t launch_transpose_kv_f32(const attn_bwd_params& p, const float* X, float* xt,
-                                    int sk_pad, cudaStream_t stream);
 
 constexpr float kHardMask = -1.0e30f;     // a mask value at or below this hides the pair
 constexpr float kEmptyRowLse = 3.0e38f;   // LSE of a row with no probability mass

@@ -7,10 +7,6 @@
 //                   the fp32 dQ accumulator row.  One
 //                   group of D*esize/16 threads per row, 16-byte loads,
 //                   shuffle reduction inside the group.
-//  prep_f32_kernel  the same for fp32 in one pass, plus the TF32-rounded
-//                   transposes [B*H][D][S_pad] of Q, dO and K that the TF32
-//                   products read (the tensor cores take TF32 operands
-//                   K-major only).
 //  dq_convert       fp32 dQ accumulator -> bf16 dQ (round to nearest even).
 //  dropout_mask     the keep mask of one (b, h) slice, for bit-exact tests.
 #include <cuda_bf16.h>
@@ -97,95 +93,6 @@ cudaError_t prep_impl(const attn_bwd_params& p, const void* O, const void* dO, c
   return cudaGetLastError();
 }
 
-// fp32 prepare in one pass.  One 256-thread block per 32-row tile of one
-// (batch, head) of the query side -- Delta, -LSE*log2(e), zeroed dQ rows and
-// the TF32-rounded transposes Q^T, dO^T -- or of the key side (K^T).  Rows are
-// read once with 16-byte loads; transposes go through padded shared memory and
-// leave as 16-byte stores along the sequence.
-template <int D>
-__global__ void __launch_bounds__(256) prep_f32_kernel(
-    const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ O,
-    const float* __restrict__ dO, const float* __restrict__ LSE, float* __restrict__ delta,
-    float* __restrict__ nlse, float* __restrict__ dq, float* __restrict__ qt,
-    float* __restrict__ dot, float* __restrict__ kt, int B, int H, int Hkv, int Sq, int Sk,
-    int sq_pad, int sk_pad, int layout, int nq_blocks) {
-  constexpr int LD = D + 1;  // padded row stride: column reads hit 32 banks
-  constexpr int C4 = D / 4;  // float4 per row
-  __shared__ float t0[32 * LD];
-  __shared__ float t1[32 * LD];
-  const int tid = threadIdx.x;
-  const bool qside = (int)blockIdx.x < nq_blocks;
-  const int blk = qside ? blockIdx.x : blockIdx.x - nq_blocks;
-  const int S = qside ? Sq : Sk, s_pad = qside ? sq_pad : sk_pad, Hx = qside ? H : Hkv;
-  const int tiles = s_pad / 32;
-  const int bh = blk / tiles, s0 = (blk % tiles) * 32;
-  const int b = bh / Hx, h = bh % Hx;
-  // row loads: thread -> (row r, float4 column c) pairs
-  for (int idx = tid; idx < 32 * C4; idx += 256) {
-    const int r = idx / C4, c = idx % C4, s = s0 + r;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), g = x;
-    if (s < S) {
-      const long long off = row_offset(layout, b, h, s, Hx, S, D) + 4 * c;
-      if (qside) {
-        x = *reinterpret_cast<const float4*>(Q + off);
-        g = *reinterpret_cast<const float4*>(dO + off);
-      } else {
-        x = *reinterpret_cast<const float4*>(K + off);
-      }
-    }
-    float* a0 = t0 + r * LD + 4 * c;
-    a0[0] = x.x; a0[1] = x.y; a0[2] = x.z; a0[3] = x.w;
-    if (qside) {
-      float* a1 = t1 + r * LD + 4 * c;
-      a1[0] = g.x; a1[1] = g.y; a1[2] = g.z; a1[3] = g.w;
-    }
-  }
-  if (qside) {
-    // Delta = dO . O per row: C4 threads per row (a power of two <= 32, so
-    // the shuffle groups never straddle a warp), then zero the dQ row
-    for (int idx = tid; idx < 32 * C4; idx += 256) {
-      const int r = idx / C4, c = idx % C4, s = s0 + r;
-      float acc = 0.f;
-      if (s < S) {
-        const long long off = row_offset(layout, b, h, s, H, S, D) + 4 * c;
-        const float4 o = *reinterpret_cast<const float4*>(O + off);
-        const float4 g = *reinterpret_cast<const float4*>(dO + off);
-        acc = o.x * g.x + o.y * g.y + o.z * g.z + o.w * g.w;
-        *reinterpret_cast<float4*>(dq + off) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int m = C4 / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, C4);
-      if (c == 0) {
-        const long long w = (long long)bh * sq_pad + s;
-        delta[w] = s < S ? acc : 0.f;
-        if (LSE)
-          nlse[w] = s < S ? -LSE[(long long)bh * Sq + s] * kLog2e : __int_as_float(0xff800000);
-      }
-    }
-  }
-  __syncthreads();
-  // transposed, TF32-rounded stores: out[bh][d][s0 .. s0 + 31]
-  float* out0 = qside ? qt : kt;
-  for (int idx = tid; idx < D * 8; idx += 256) {
-    const int d = idx / 8, k = idx % 8;  // 8 float4 cover the 32 rows
-    const long long o = ((long long)bh * D + d) * s_pad + s0 + 4 * k;
-    float4 v;
-    v.x = __uint_as_float(__float_as_uint(t0[(4 * k + 0) * LD + d]) + 0x1000u);
-    v.y = __uint_as_float(__float_as_uint(t0[(4 * k + 1) * LD + d]) + 0x1000u);
-    v.z = __uint_as_float(__float_as_uint(t0[(4 * k + 2) * LD + d]) + 0x1000u);
-    v.w = __uint_as_float(__float_as_uint(t0[(4 * k + 3) * LD + d]) + 0x1000u);
-    *reinterpret_cast<float4*>(out0 + o) = v;
-    if (qside) {
-      float4 u;
-      u.x = __uint_as_float(__float_as_uint(t1[(4 * k + 0) * LD + d]) + 0x1000u);
-      u.y = __uint_as_float(__float_as_uint(t1[(4 * k + 1) * LD + d]) + 0x1000u);
-      u.z = __uint_as_float(__float_as_uint(t1[(4 * k + 2) * LD + d]) + 0x1000u);
-      u.w = __uint_as_float(__float_as_uint(t1[(4 * k + 3) * LD + d]) + 0x1000u);
-      *reinterpret_cast<float4*>(dot + o) = u;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src,
                                                          uint2* __restrict__ dst, long long n4) {
   for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n4;
@@ -220,24 +127,6 @@ cudaError_t launch_prep(const attn_bwd_params& p, const void* O, const void* dO,
               : prep_impl<false, 64>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream);
   return bf ? prep_impl<true, 128>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream)
             : prep_impl<false, 128>(p, O, dO, LSE, delta, lse2, sq_pad, dq_acc, stream);
-}
-
-cudaError_t launch_prep_f32(const attn_bwd_params& p, const float* Q, const float* K,
-                            const float* O, const float* dO, const float* LSE, float* delta,
-                            float* nlse, float* dq, float* qt, float* dot, float* kt, int sq_pad,
-                            int sk_pad, cudaStream_t stream) {
-  const int nq = p.batch * p.num_heads * (sq_pad / 32);
-  const int nk = p.batch * p.num_kv_heads * (sk_pad / 32);
-  if (p.head_dim == 64)
-    prep_f32_kernel<64><<<nq + nk, 256, 0, stream>>>(Q, K, O, dO, LSE, delta, nlse, dq, qt, dot, kt,
-                                                     p.batch, p.num_heads, p.num_kv_heads, p.seq_q,
-                                                     p.seq_k, sq_pad, sk_pad, p.layout, nq);
-  else
-    prep_f32_kernel<128><<<nq + nk, 256, 0, stream>>>(Q, K, O, dO, LSE, delta, nlse, dq, qt, dot,
-                                                      kt, p.batch, p.num_heads, p.num_kv_heads,
-                                                      p.seq_q, p.seq_k, sq_pad, sk_pad, p.layout,
-                                                      nq);
-  return cudaGetLastError();
 }
 
 namespace {
@@ -343,23 +232,6 @@ cudaError_t launch_dq_reduce(const attn_bwd_params& p, const float* slices, void
               : dq_reduce_impl<false, 64>(p, slices, dQ, bn, bm, stream);
   return bf ? dq_reduce_impl<true, 128>(p, slices, dQ, bn, bm, stream)
             : dq_reduce_impl<false, 128>(p, slices, dQ, bn, bm, stream);
-}
-
-cudaError_t launch_transpose_kv_f32(const attn_bwd_params& p, const float* X, float* xt,
-                                    int sk_pad, cudaStream_t stream) {
-  // key-side blocks of the fp32 prepare only (no query-side blocks)
-  const int nk = p.batch * p.num_kv_heads * (sk_pad / 32);
-  if (p.head_dim == 64)
-    prep_f32_kernel<64><<<nk, 256, 0, stream>>>(nullptr, X, nullptr, nullptr, nullptr, nullptr,
-                                                nullptr, nullptr, nullptr, nullptr, xt, p.batch,
-                                                p.num_heads, p.num_kv_heads, p.seq_q, p.seq_k, 0,
-                                                sk_pad, p.layout, 0);
-  else
-    prep_f32_kernel<128><<<nk, 256, 0, stream>>>(nullptr, X, nullptr, nullptr, nullptr, nullptr,
-                                                 nullptr, nullptr, nullptr, nullptr, xt, p.batch,
-                                                 p.num_heads, p.num_kv_heads, p.seq_q, p.seq_k, 0,
-                                                 sk_pad, p.layout, 0);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const attn_bwd_params& p, const float* dq_acc, void* dQ,

@@ -220,15 +220,30 @@ __device__ __forceinline__ void tc_fence_after() {
 // Shared-memory matrix descriptor (tcgen05 "matrix descriptor"):
 //   [0,14)  start address >> 4      [16,30) leading byte offset >> 4
 //   [32,46) stride byte offset >> 4 [46,48) version = 1
-//   [49,52) base offset = 0         [61,64) layout: 2 = 128-byte swizzle
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   [49,52) base offset = 0         [61,64) layout: 2 = 128-byte swizzle,
+//                                           1 = 128-byte swizzle of 32-byte atoms
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= (uint64_t)layout << 61;
   return d;
+}
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, 2);
+}
+// MN-major TF32 operand: [MN / 32 blocks][K rows][128 bytes = 32 MN elements],
+// each row's 32-byte chunks swapped by XOR with (row & 3) -- what TMA writes
+// with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B.  The tensor cores read a K step
+// of 8 rows as two groups of four: LBO = bytes between 32-element MN blocks,
+// SBO = 512 (four rows); the next K step starts 1024 bytes further on.
+// (Measured on sm_103a: with this descriptor every (MN, K) element of a
+// coded tile lands where a plain product puts it.)
+__device__ __forceinline__ uint64_t mn32_desc(uint32_t saddr, uint32_t lbo) {
+  return smem_desc(saddr, lbo, 512, 1);
 }
 
 // Instruction descriptor for kind::tf32 / kind::f16 (dense, fp32 accumulate):

@@ -140,9 +140,8 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
  * arguments and rules as attn_bwd):
  *  attn_bwd_prepare  per-row Delta_i = dO_i . O_i (the Metal page's
  *                    "D = rowsum(dO * O)") and LSE * log2(e) into the
- *                    workspace, zeroes the fp32 dQ accumulator, and for fp32
- *                    writes the TF32-rounded transposed copies Q^T, dO^T, K^T
- *                    the tensor-core products read.
+ *                    workspace and zeroes the fp32 dQ accumulator (fp32:
+ *                    dQ itself).
  *  attn_bwd_tiles    the fused tile kernel: recomputes P, forms dS and
  *                    produces dK, dV and the dQ accumulation.
  *  attn_bwd_finish   bf16: converts the fp32 dQ accumulator to dQ; with
@@ -188,7 +187,8 @@ attn_status attn_bwd_lse(const attn_bwd_params* p, const void* Q, const void* K,
  *   Q, K, V: p->layout, p->dtype; fp32 inputs are multiplied as TF32.
  *   mask: as for attn_bwd.  O: p->layout, p->dtype (written).  LSE: fp32
  *   [B, H, Sq] (written).  workspace: >= attn_fwd_workspace_size(p) bytes,
- *   256-byte aligned (fp32: a TF32 copy of V^T).
+ *   256-byte aligned (not written: the forward needs no scratch; the
+ *   argument is kept so that callers need not change if it ever does).
  * Device pointers, 16-byte aligned.  p->deterministic is ignored (the forward
  * has no atomics).  Errors as for attn_bwd.
  */
