@@ -129,30 +129,40 @@ CUresult make_map_dq(CUtensorMap* m, void* base, int D, int S, int H, int B, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// Natural [.., S, .., D] tensor in boxes of 128 bytes x box_rows, 128-byte
-// swizzle (K-major operand tiles); atom32 (fp32 only): the 128-byte swizzle of
-// 32-byte atoms, the layout of a TF32 operand read MN-major.
+// Natural [.., S, .., D] tensor as a whole-tile operand map.  The D columns
+// are split into W-element column blocks (W = 128 bytes of elements) that
+// form a dimension of their own, after the rows: dims {W, S, D / W, H, B}.
+// One box {W, box_rows, D / W} then lands in shared memory as
+// [D / W][box_rows][W], the column-block layout of the operand tiles, in a
+// single copy (one copy per tile instead of one per column block: measured
+// ~10 % faster for the fp32 D = 128 tile kernel, which issues several tile
+// copies per query tile).  128-byte swizzle (K-major operand tiles); atom32
+// (fp32 only): the 128-byte swizzle of 32-byte atoms, the layout of a TF32
+// operand read MN-major.  fp32 tensors are fetched as TF32.
 CUresult make_map(CUtensorMap* m, const void* base, int dtype, int D, int S, int H, int B,
                   int layout, int box_rows, bool atom32 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
   const int e = dtype == ATTN_BF16 ? 2 : 4;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
-  cuuint64_t strides[3];
+  const int W = 128 / e;
+  cuuint64_t dims[5] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)(D / W), (cuuint64_t)H,
+                        (cuuint64_t)B};
+  cuuint64_t strides[4];  // bytes, dims 1..4
   if (layout == ATTN_LAYOUT_BHSD) {
     strides[0] = (cuuint64_t)D * e;
-    strides[1] = (cuuint64_t)S * D * e;
-    strides[2] = (cuuint64_t)H * S * D * e;
+    strides[1] = 128;
+    strides[2] = (cuuint64_t)S * D * e;
+    strides[3] = (cuuint64_t)H * S * D * e;
   } else {
     strides[0] = (cuuint64_t)H * D * e;
-    strides[1] = (cuuint64_t)D * e;
-    strides[2] = (cuuint64_t)S * H * D * e;
+    strides[1] = 128;
+    strides[2] = (cuuint64_t)D * e;
+    strides[3] = (cuuint64_t)S * H * D * e;
   }
-  cuuint32_t box[4] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  // fp32 tensors are fetched as TF32 (the operand type of the products)
+  cuuint32_t box[5] = {(cuuint32_t)W, (cuuint32_t)box_rows, (cuuint32_t)(D / W), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_TFLOAT32,
-             4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             5, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }

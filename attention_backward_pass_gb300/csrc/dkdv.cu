@@ -125,7 +125,6 @@ struct Layout {
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
   static constexpr int W = 128 / E;       // elements per 128-byte segment
   static constexpr int KSTEP = 32 / E;    // K elements per MMA instruction
-  static constexpr int NB_D = D / W;      // column blocks of a D-wide row tile
   static constexpr int K_BYTES = BN * D * E;
   static constexpr int Q_BYTES = BM * D * E;
   static constexpr int P_BYTES = BN * BM * E;
@@ -535,18 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       mbar_expect_tx(kv_full, L::KV_TX);
-      for (int cb = 0; cb < L::NB_D; ++cb) {
-        tma_load_4d(smem + L::OFF_K + cb * BN * 128, &tm_k, kv_full, cb * W, w.k0, w.kvh, w.b);
-        if constexpr (!L::VGL)
-          tma_load_4d(smem + L::OFF_VLOAD + cb * BN * 128, &tm_v, kv_full, cb * W, w.k0, w.kvh,
-                      w.b);
-      }
-      if constexpr (L::KMAJ) {
-        // MN-major copy of K for GEMM5: [D / W blocks][BN keys][W columns]
-        for (int cb = 0; cb < L::NB_D; ++cb)
-          tma_load_4d(smem + L::OFF_KT + cb * BN * 128, &tm_kt, kv_full, cb * W, w.k0, w.kvh,
-                      w.b);
-      }
+      // whole tiles [D / W column blocks][BN keys][W], one copy each
+      tma_load_5d(smem + L::OFF_K, &tm_k, kv_full, 0, w.k0, 0, w.kvh, w.b);
+      if constexpr (!L::VGL)
+        tma_load_5d(smem + L::OFF_VLOAD, &tm_v, kv_full, 0, w.k0, 0, w.kvh, w.b);
+      if constexpr (L::KMAJ)  // MN-major copy of K for GEMM5
+        tma_load_5d(smem + L::OFF_KT, &tm_kt, kv_full, 0, w.k0, 0, w.kvh, w.b);
       int nat_issued = 0, row_issued = 0, do_issued = 0;
       for (int t = 0; t < T; ++t) {
         const int g = t / w.tiles_per_head;
@@ -558,22 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = t % NAT;
         if (t >= NAT && !mbar_wait(&nat_empty[s], ((t / NAT) - 1) & 1, a.err)) break;
         mbar_expect_tx(&nat_full[s], L::NAT_TX);
-        for (int cb = 0; cb < L::NB_D; ++cb) {
-          tma_load_4d(smem + L::OFF_Q + s * L::NAT_STRIDE + cb * BM * 128, &tm_q, &nat_full[s],
-                      cb * W, q0, h, w.b);
-          if constexpr (!L::SPLITQ)
-            tma_load_4d(smem + L::OFF_DO + s * L::NAT_STRIDE + cb * BM * 128, &tm_do,
-                        &nat_full[s], cb * W, q0, h, w.b);
-        }
+        tma_load_5d(smem + L::OFF_Q + s * L::NAT_STRIDE, &tm_q, &nat_full[s], 0, q0, 0, h, w.b);
+        if constexpr (!L::SPLITQ)
+          tma_load_5d(smem + L::OFF_DO + s * L::NAT_STRIDE, &tm_do, &nat_full[s], 0, q0, 0, h,
+                      w.b);
         nat_issued = t + 1;
         if constexpr (L::SPLITQ) {
           // dO slot of its own, released by GEMM2
           const int so = t % L::NDO;
           if (t >= L::NDO && !mbar_wait(&do_empty[so], ((t / L::NDO) - 1) & 1, a.err)) break;
           mbar_expect_tx(&do_full[so], L::Q_BYTES);
-          for (int cb = 0; cb < L::NB_D; ++cb)
-            tma_load_4d(smem + L::OFF_DO + so * L::Q_BYTES + cb * BM * 128, &tm_do, &do_full[so],
-                        cb * W, q0, h, w.b);
+          tma_load_5d(smem + L::OFF_DO + so * L::Q_BYTES, &tm_do, &do_full[so], 0, q0, 0, h, w.b);
           do_issued = t + 1;
         }
         // LSE2 / Delta rows of the tile: a ring of their own, released by the
@@ -615,12 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = t % TR;
           if (t >= TR && !mbar_wait(&tr_empty[r], ((t / TR) - 1) & 1, a.err)) break;
           mbar_expect_tx(&tr_full[r], L::TR_TX);
-          for (int cb = 0; cb < L::NB_D; ++cb) {
-            tma_load_4d(smem + L::OFF_QT + r * L::Q_BYTES + cb * BM * 128, &tm_qt, &tr_full[r],
-                        cb * W, q0, h, w.b);
-            tma_load_4d(smem + L::OFF_DOT + r * L::Q_BYTES + cb * BM * 128, &tm_dot, &tr_full[r],
-                        cb * W, q0, h, w.b);
-          }
+          tma_load_5d(smem + L::OFF_QT + r * L::Q_BYTES, &tm_qt, &tr_full[r], 0, q0, 0, h, w.b);
+          tma_load_5d(smem + L::OFF_DOT + r * L::Q_BYTES, &tm_dot, &tr_full[r], 0, q0, 0, h, w.b);
           tr_issued = t + 1;
         }
         for (int t = (tr_issued > TR ? tr_issued - TR : 0); t < tr_issued; ++t)

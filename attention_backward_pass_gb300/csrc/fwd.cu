@@ -53,7 +53,6 @@ struct FwdLayout {
   static constexpr int BN = (!BF16 && D == 128) ? 64 : 128;  // keys per tile
   static constexpr int W = 128 / E;     // elements per 128-byte segment
   static constexpr int KSTEP = 32 / E;  // K elements per MMA instruction
-  static constexpr int NB_D = D / W;    // column blocks of a D-wide row tile
   static constexpr int Q_BYTES = BM * D * E;
   static constexpr int K_BYTES = BN * D * E;
   static constexpr int V_BYTES = BN * D * E;  // [BN][D] (bf16) or [D][BN] (fp32)
@@ -153,7 +152,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = FwdLayout<BF16, D>;
   constexpr int BM = L::BM, BN = L::BN, NK = L::NK, NV = L::NV, NSB = L::NSB, NQ = L::NQ,
-                W = L::W, QC = L::QC, OC = L::OC;
+                QC = L::QC, OC = L::OC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -223,9 +222,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int qb = nz % NQ;
         if (nz >= NQ && !mbar_wait(&q_empty[qb], ((nz / NQ) - 1) & 1, a.err)) break;
         mbar_expect_tx(&q_full[qb], L::Q_BYTES);
-        for (int cb = 0; cb < L::NB_D; ++cb)
-          tma_load_4d(smem + L::OFF_Q + qb * L::Q_BYTES + cb * BM * 128, &tm_q, &q_full[qb],
-                      cb * W, it.q0, it.h, it.b);
+        tma_load_5d(smem + L::OFF_Q + qb * L::Q_BYTES, &tm_q, &q_full[qb], 0, it.q0, 0, it.h,
+                    it.b);
         ++nz;
         const int kvh = it.h / a.group;
         for (int t = 0; t < it.T; ++t) {
@@ -236,9 +234,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             break;
           }
           mbar_expect_tx(&k_full[sk], L::K_BYTES);
-          for (int cb = 0; cb < L::NB_D; ++cb)
-            tma_load_4d(smem + L::OFF_K + sk * L::K_BYTES + cb * BN * 128, &tm_k, &k_full[sk],
-                        cb * W, k0, kvh, it.b);
+          tma_load_5d(smem + L::OFF_K + sk * L::K_BYTES, &tm_k, &k_full[sk], 0, k0, 0, kvh, it.b);
           ++gk;
           const int sv = gv % NV;
           if (gv >= NV && !mbar_wait(&v_empty[sv], ((gv / NV) - 1) & 1, a.err)) {
@@ -246,10 +242,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             break;
           }
           mbar_expect_tx(&v_full[sv], L::V_BYTES);
-          // natural V [BN keys][D]: column blocks of W elements
-          for (int cb = 0; cb < L::NB_D; ++cb)
-            tma_load_4d(smem + L::OFF_V + sv * L::V_BYTES + cb * BN * 128, &tm_v, &v_full[sv],
-                        cb * W, k0, kvh, it.b);
+          // natural V [D / W column blocks][BN keys][W]
+          tma_load_5d(smem + L::OFF_V + sv * L::V_BYTES, &tm_v, &v_full[sv], 0, k0, 0, kvh, it.b);
           ++gv;
         }
       }

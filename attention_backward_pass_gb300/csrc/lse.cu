@@ -48,7 +48,6 @@ struct LseLayout {
   static constexpr int BN = (!BF16 && D == 128) ? 64 : 128;
   static constexpr int W = 128 / E;      // elements per 128-byte segment
   static constexpr int KSTEP = 32 / E;   // K elements per MMA instruction
-  static constexpr int NB_D = D / W;     // column blocks of a D-wide row tile
   static constexpr int Q_BYTES = BM * D * E;
   static constexpr int K_BYTES = BN * D * E;
   static constexpr int NQ = 2;           // Q buffers
@@ -241,7 +240,7 @@ __global__ void __launch_bounds__(kLseThreads, 1)
     lse_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const LseArgs a) {
   using L = LseLayout<BF16, D>;
-  constexpr int BM = L::BM, BN = L::BN, NK = L::NK, NSB = L::NSB, NQ = L::NQ, W = L::W,
+  constexpr int BM = L::BM, BN = L::BN, NK = L::NK, NSB = L::NSB, NQ = L::NQ,
                 QC = L::QC, QC2 = L::QC2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -302,9 +301,8 @@ __global__ void __launch_bounds__(kLseThreads, 1)
         const int qb = nz % NQ;
         if (nz >= NQ && !mbar_wait(&q_empty[qb], ((nz / NQ) - 1) & 1, a.err)) break;
         mbar_expect_tx(&q_full[qb], L::Q_BYTES);
-        for (int cb = 0; cb < L::NB_D; ++cb)
-          tma_load_4d(smem + L::OFF_Q + qb * L::Q_BYTES + cb * BM * 128, &tm_q, &q_full[qb],
-                      cb * W, it.q0, it.h, it.b);
+        tma_load_5d(smem + L::OFF_Q + qb * L::Q_BYTES, &tm_q, &q_full[qb], 0, it.q0, 0, it.h,
+                    it.b);
         ++nz;
         const int kvh = it.h / a.group;
         for (int t = 0; t < it.T; ++t, ++g) {
@@ -314,9 +312,8 @@ __global__ void __launch_bounds__(kLseThreads, 1)
             break;
           }
           mbar_expect_tx(&k_full[s], L::K_BYTES);
-          for (int cb = 0; cb < L::NB_D; ++cb)
-            tma_load_4d(smem + L::OFF_K + s * L::K_BYTES + cb * BN * 128, &tm_k, &k_full[s],
-                        cb * W, it.k_start + t * BN, kvh, it.b);
+          tma_load_5d(smem + L::OFF_K + s * L::K_BYTES, &tm_k, &k_full[s], 0, it.k_start + t * BN,
+                      0, kvh, it.b);
         }
       }
       // let every copy still in flight land before the CTA can exit
