@@ -52,6 +52,19 @@ SMALL = {
                                     head_dim=128, scale=1 / np.sqrt(128), causal=1,
                                     causal_offset=120, has_mask=1, dropout_prob=0.2,
                                     seed=0x5EED0008, layout=W.LAYOUT_BSHD),
+    # more work items (key tile, batch, KV head) than SMs, so CTAs walk several
+    # items: D = 64 causal (192 items), GQA window D = 128 (176 items), items
+    # without query tiles mixed in (448 of 576 see no query: their dK / dV are
+    # zeros), mask + dropout across items (192 items)
+    "many_items_d64": P(batch=8, num_heads=8, num_kv_heads=8, seq_q=380, seq_k=380, causal=1),
+    "many_items_gqa_window_d128": P(batch=4, num_heads=8, num_kv_heads=4, seq_q=1300,
+                                    seq_k=1300, head_dim=128, scale=1 / np.sqrt(128), causal=1,
+                                    window=500, layout=W.LAYOUT_BSHD),
+    "many_items_empty_keys": P(batch=4, num_heads=16, num_kv_heads=16, seq_q=200, seq_k=1100,
+                               causal=1),
+    "many_items_mask_dropout": P(batch=4, num_heads=8, num_kv_heads=8, seq_q=256, seq_k=700,
+                                 causal=1, causal_offset=444, has_mask=1, dropout_prob=0.1,
+                                 seed=0x5EED0009),
 }
 
 
