@@ -891,14 +891,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-      if (!warp_wait(&s_full[b], (t / NSB) & 1, a.err) ||
-          !warp_wait(&row_full[rs], (t / RST) & 1, a.err)) {
+      // the tile's -LSE*log2(e) / Delta rows land well ahead of its scores:
+      // wait for them first and (one 16-column chunk per thread) take this
+      // half's values into registers while GEMM1/2 still run, so the
+      // arithmetic after s_full reads no shared memory for them
+      if (!warp_wait(&row_full[rs], (t / RST) & 1, a.err)) {
+        ok = false;
+        break;
+      }
+      const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + rs * BM * 4);
+      const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + rs * BM * 4);
+      constexpr bool PRE = L::COLS == 16;  // fp32, D = 128
+      uint64_t nlr[PRE ? 8 : 1], dlr[PRE ? 8 : 1];
+      if constexpr (PRE) {
+        const uint64_t* n2 = reinterpret_cast<const uint64_t*>(sLSE + cbeg);
+        const uint64_t* d2 = reinterpret_cast<const uint64_t*>(sDelta + cbeg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          nlr[i] = n2[i];
+          dlr[i] = d2[i];
+        }
+      }
+      if (!warp_wait(&s_full[b], (t / NSB) & 1, a.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* sLSE = reinterpret_cast<const float*>(smem + L::OFF_LSE + rs * BM * 4);
-      const float* sDelta = reinterpret_cast<const float*>(smem + L::OFF_DELTA + rs * BM * 4);
       const bool plain = tile_is_plain(a, q0, BM, w.k0, BN);
       const uint32_t t_s = tmem + lane_base + b * 2 * BM, t_dp = t_s + BM;
       const uint32_t t_p = L::INPL ? t_s : tmem + lane_base + L::T_P + pb * L::PCOLS;
@@ -935,8 +953,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j >= 0) {
             if (!a.has_mask && !a.dropout) {
               // two queries at a time with packed fp32x2 arithmetic
-              const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(sLSE + c0);
-              const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(sDelta + c0);
+              const uint64_t* nl2 = PRE ? nlr : reinterpret_cast<const uint64_t*>(sLSE + c0);
+              const uint64_t* dl2 = PRE ? dlr : reinterpret_cast<const uint64_t*>(sDelta + c0);
               const uint64_t c2 = pk2(a.scale_log2e, a.scale_log2e);
               const uint64_t sc2 = pk2(a.scale, a.scale);
 #pragma unroll
