@@ -362,9 +362,17 @@ attn_status attn_bwd_lse(const attn_bwd_params* p, const void* Q, const void* K,
   return run_lse(p, Q, K, mask, LSE, 0, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
-attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
-                           const void* dO, const float* mask, void* dQ, void* dK, void* dV,
-                           void* workspace, size_t workspace_bytes, void* stream_v) {
+namespace {
+
+// The tile stage.  after_prepare: launched right after this library's own
+// prepare kernel on the same stream, so it may start while that kernel
+// finishes (programmatic dependent launch; everything that reads the
+// prepare's outputs waits for it first).  A direct attn_bwd_tiles call
+// follows whatever the caller ran last and launches normally.
+attn_status tiles_impl(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                       const void* dO, const float* mask, void* dQ, void* dK, void* dV,
+                       void* workspace, size_t workspace_bytes, void* stream_v,
+                       bool after_prepare) {
   Plan pl;
   attn_status st = make_plan(p, dQ, workspace, workspace_bytes, &pl);
   if (st != ATTN_OK) return st;
@@ -440,8 +448,16 @@ attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* 
   a.V = V;
   a.n_kv_tiles = (p->seq_k + bn - 1) / bn;
   a.err = err;
-  if (launch_dkdv(*p, maps, a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_dkdv(*p, maps, a, stream, after_prepare) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status attn_bwd_tiles(const attn_bwd_params* p, const void* Q, const void* K, const void* V,
+                           const void* dO, const float* mask, void* dQ, void* dK, void* dV,
+                           void* workspace, size_t workspace_bytes, void* stream_v) {
+  return tiles_impl(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, workspace_bytes, stream_v, false);
 }
 
 attn_status attn_bwd_finish(const attn_bwd_params* p, void* dQ, void* workspace,
@@ -480,7 +496,7 @@ attn_status attn_bwd(const attn_bwd_params* p, const void* Q, const void* K, con
   }
   st = prepare_impl(p, Q, K, O, dO, LSE, dQ, workspace, workspace_bytes, stream);
   if (st != ATTN_OK) return st;
-  st = attn_bwd_tiles(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, workspace_bytes, stream);
+  st = tiles_impl(p, Q, K, V, dO, mask, dQ, dK, dV, workspace, workspace_bytes, stream, true);
   if (st != ATTN_OK) return st;
   return attn_bwd_finish(p, dQ, workspace, workspace_bytes, stream);
 }

@@ -567,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // LSE2 / Delta rows of the tile: a ring of their own, released by the
         // softmax warps as soon as they finish the tile
         const int rr = t % RST;
+        if (t == 0 && a.pdl) griddep_wait();  // the rows are written by the prepare kernel
         if (t >= RST && !mbar_wait(&row_empty[rr], ((t / RST) - 1) & 1, a.err)) break;
         mbar_expect_tx(&row_full[rr], L::ROW_TX);
         bulk_load(smem + L::OFF_LSE + rr * BM * 4, a.lse2 + row, BM * 4, &row_full[rr]);
@@ -1213,6 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
       // every dQ thread is also done reading the staging tile of tile t-1
       if (!dq_group_all(mbar_wait(mma5_done, t & 1, a.err))) break;
+      if (t == 0 && a.pdl) griddep_wait();  // the accumulator is zeroed by the prepare kernel
       tc_fence_after();
       __syncwarp();  // tcgen05.ld is warp-collective; the staging below diverges on r
       // (DQA) the accumulator of tile t sits in the P columns of its buffer
@@ -1305,15 +1307,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool BF16, int D>
-cudaError_t launch_impl(const TileMaps& m, const TileArgs& a, cudaStream_t stream) {
+cudaError_t launch_impl(const TileMaps& m, const TileArgs& a0, cudaStream_t stream, bool pdl) {
+  TileArgs a = a0;
+  a.pdl = pdl ? 1 : 0;
   using L = Layout<BF16, D>;
   auto kern = dkdv_kernel<BF16, D>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = a.n_kv_tiles * a.B * a.Hkv;
-  kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, m.dq,
-                                                  a);
+  if (!pdl) {
+    kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot,
+                                                    m.dq, a);
+    return cudaGetLastError();
+  }
+  // may start while the prepare kernel finishes: key tiles, query tiles and
+  // GEMM1/2 need nothing it writes; the LSE / Delta rows and the dQ
+  // accumulator are touched only after griddep_wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, m.dq, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1339,13 +1361,15 @@ int dkdv_block_n(int dtype, int head_dim) {
 }
 
 cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool after_prepare) {
   if (p.dtype == ATTN_BF16) {
-    return p.head_dim == 64 ? launch_impl<true, 64>(maps, a, stream)
-                            : launch_impl<true, 128>(maps, a, stream);
+    return p.head_dim == 64 ? launch_impl<true, 64>(maps, a, stream, after_prepare)
+                            : launch_impl<true, 128>(maps, a, stream, after_prepare);
   }
-  return p.head_dim == 64 ? launch_impl<false, 64>(maps, a, stream)
-                          : launch_impl<false, 128>(maps, a, stream);
+  // (fp32, D = 128 launches normally: as a dependent its first wave competed
+  // with the prepare kernel's tail and the step was 0.7 % slower)
+  return p.head_dim == 64 ? launch_impl<false, 64>(maps, a, stream, after_prepare)
+                          : launch_impl<false, 128>(maps, a, stream, false);
 }
 
 }  // namespace attnbwd

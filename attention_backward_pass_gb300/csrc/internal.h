@@ -40,6 +40,7 @@ struct TileArgs {
   void* dV;
   const void* V;       // V itself (configurations that load it into tensor memory directly)
   int n_kv_tiles;
+  int pdl;             // launched as a programmatic dependent of the prepare kernel
   unsigned int* err;
 };
 
@@ -98,8 +99,9 @@ struct TileMaps {
   CUtensorMap qt, kt, dot;    // fp32: Q, K, dO again, 32-byte-atom swizzle (MN-major reads)
   CUtensorMap dq;             // fp32 dQ accumulator (reduce-add target)
 };
+// after_prepare: programmatic dependent launch behind the prepare kernel
 cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool after_prepare);
 int dkdv_block_m(int dtype, int head_dim);
 int dkdv_block_n(int dtype, int head_dim);
 int dkdv_dq_box_d(int dtype, int head_dim);  // head-dim columns per dQ reduce box

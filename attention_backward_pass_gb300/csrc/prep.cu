@@ -14,6 +14,7 @@
 
 #include "internal.h"
 #include "philox.cuh"
+#include "ptx.cuh"
 
 namespace attnbwd {
 
@@ -30,6 +31,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const void* __restrict__ O,
   constexpr int E = BF16 ? 2 : 4;
   constexpr int G = D * E / 16;  // threads per row
   constexpr int ROWS = 256 / G;
+  // the tile kernel behind this one may start its CTAs once every block has
+  // started (it waits for this kernel before it reads anything written here)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int sub = threadIdx.x % G;
   const long long r = (long long)blockIdx.x * ROWS + threadIdx.x / G;
   const long long nrows = (long long)B * H * sq_pad;
