@@ -55,7 +55,7 @@ struct FwdLayout {
   static constexpr int KSTEP = 32 / E;  // K elements per MMA instruction
   static constexpr int Q_BYTES = BM * D * E;
   static constexpr int K_BYTES = BN * D * E;
-  static constexpr int V_BYTES = BN * D * E;  // [BN][D] (bf16) or [D][BN] (fp32)
+  static constexpr int V_BYTES = BN * D * E;  // [D / W column blocks][BN][W]
   static constexpr int NQ = (!BF16 && D == 128) ? 1 : 2;
   static constexpr int NK = 2, NV = 2, NSB = 2;
   static constexpr int QC = BN / 4;  // key columns per softmax thread
@@ -97,6 +97,26 @@ __device__ __forceinline__ float fwd_ex2(float x) {
 }
 
 __device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+// packed fp32x2 arithmetic (sm_100+)
+__device__ __forceinline__ uint64_t fpk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void fup2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ff2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t ff2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t fwd_pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -401,11 +421,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         float x[QC];
         float pm = -INFINITY;
+        // a share without mask or dropout that lies wholly inside the row's
+        // visible keys needs no per-key test: two scores per packed multiply
+        const bool plain = !mrow && !a.dropout && kb >= lo && kb + QC <= hi;
+        if (plain) {
+          const uint64_t c2 = fpk2(c, c);
 #pragma unroll
-        for (int e = 0; e < QC; ++e) {
-          const bool vis = (unsigned)(kb + e - lo) < (unsigned)(hi - lo) && mv[e] > kHardMask;
-          x[e] = vis ? fmaf(__uint_as_float(sv[e]), c, mv[e] * kLog2e) : -INFINITY;
-          pm = fmaxf(pm, x[e]);
+          for (int e = 0; e < QC; e += 2)
+            fup2(ff2mul(fpk2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2), x[e],
+                 x[e + 1]);
+#pragma unroll
+          for (int e = 0; e < QC; ++e) pm = fmaxf(pm, x[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < QC; ++e) {
+            const bool vis = (unsigned)(kb + e - lo) < (unsigned)(hi - lo) && mv[e] > kHardMask;
+            x[e] = vis ? fmaf(__uint_as_float(sv[e]), c, mv[e] * kLog2e) : -INFINITY;
+            pm = fmaxf(pm, x[e]);
+          }
         }
         // the row's maximum over the tile: the four shares meet in shared
         // memory (double-buffered by tile parity); every softmax thread
@@ -479,11 +512,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // and P o M written over this share's S columns
         uint32_t pw[QC];
         float ls = 0.f;
+        if (m == -INFINITY) {  // nothing visible in the row so far
 #pragma unroll
-        for (int e = 0; e < QC; ++e) {
-          const float pe = m == -INFINITY ? 0.f : fwd_ex2(x[e] - m);
-          ls += pe;
-          pw[e] = __float_as_uint(((keep >> e) & 1u) ? pe * mul : 0.f);
+          for (int e = 0; e < QC; ++e) pw[e] = 0u;
+        } else if (!a.dropout) {
+          // x - m two at a time (exp2(-inf) = 0 for hidden keys), partial sums in pairs
+          const uint64_t nm2 = fpk2(-m, -m);
+          uint64_t ls2 = fpk2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < QC; e += 2) {
+            float d0, d1;
+            fup2(ff2add(fpk2(x[e], x[e + 1]), nm2), d0, d1);
+            const float p0 = fwd_ex2(d0), p1 = fwd_ex2(d1);
+            ls2 = ff2add(ls2, fpk2(p0, p1));
+            pw[e] = __float_as_uint(p0);
+            pw[e + 1] = __float_as_uint(p1);
+          }
+          float l0, l1;
+          fup2(ls2, l0, l1);
+          ls = l0 + l1;
+        } else {
+#pragma unroll
+          for (int e = 0; e < QC; ++e) {
+            const float pe = fwd_ex2(x[e] - m);
+            ls += pe;
+            pw[e] = __float_as_uint(((keep >> e) & 1u) ? pe * mul : 0.f);
+          }
         }
         l += ls;
         if (ok) {
