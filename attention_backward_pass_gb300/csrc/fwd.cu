@@ -96,7 +96,12 @@ __device__ __forceinline__ float fwd_ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// The four softmax warps of TMEM sub-partition sp (one per quarter of the key
+// columns) hold the four shares of the same 32 rows: named barrier 2 + sp
+// over their 128 threads.
+__device__ __forceinline__ void sp_sync(int sp) {
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + sp) : "memory");
+}
 
 // packed fp32x2 arithmetic (sm_100+)
 __device__ __forceinline__ uint64_t fpk2(float a, float b) {
@@ -441,10 +446,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         // the row's maximum over the tile: the four shares meet in shared
-        // memory (double-buffered by tile parity); every softmax thread
-        // reaches this barrier on every tile, also after a failed wait
+        // memory (double-buffered by tile parity); every softmax thread of the
+        // sub-partition reaches this barrier on every tile, also after a
+        // failed wait
         rmax[((g & 1) * 4 + part) * BM + r] = pm;
-        soft_sync();
+        sp_sync(sp);
         float mt = rmax[((g & 1) * 4 + 0) * BM + r];
 #pragma unroll
         for (int u = 1; u < 4; ++u) mt = fmaxf(mt, rmax[((g & 1) * 4 + u) * BM + r]);
@@ -573,7 +579,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // ---- item epilogue: merge the partial sums, read O, divide, store
       rsum[part * BM + r] = l;
-      soft_sync();
+      sp_sync(sp);
       float ll = 0.f;
 #pragma unroll
       for (int u = 0; u < 4; ++u) ll += rsum[u * BM + r];
@@ -627,7 +633,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (q_ok && part == 0)
         a.LSE[(long long)it.bh * a.Sq + q] = empty ? kEmptyRowLse : (m + log2f(ll)) * kFwdLn2;
-      soft_sync();  // rsum is reused by the next item
+      sp_sync(sp);  // rsum is reused by the next item
     }
   }
 
