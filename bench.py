@@ -1,8 +1,8 @@
 #!/usr/bin/env python
 """Throughput of the GB300 attention backward pass (dQ + dK + dV).
 
-One step = one full backward pass (attn_bwd: Delta/LSE prep, the fp32
-transposes, the fused tcgen05 tile kernel and, for bf16, the dQ conversion)
+One step = one full backward pass (attn_bwd: Delta/LSE prep, the fused
+tcgen05 tile kernel and, for bf16, the dQ conversion)
 over one batch of the chosen workload, with inputs resident in HBM.  The
 metric counts 10*D flops per visible (query, key) pair per query head (the
 five dense contractions); recomputation is not credited.
