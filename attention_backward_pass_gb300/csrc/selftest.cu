@@ -1,6 +1,7 @@
 // Tensor-core self test: one CTA computes C = A * B^T with tcgen05.mma from
 // operands staged in 128-byte-swizzled shared memory, in K-major or MN-major
-// form, and reads the accumulator back from tensor memory.  This is the
+// form (TF32 MN-major: the 128-byte swizzle of 32-byte atoms), and reads the
+// accumulator back from tensor memory.  This is the
 // building block every tile kernel of the library relies on (same descriptor
 // and swizzle helpers), checked in isolation against a CPU product.
 #include <cuda_bf16.h>
@@ -21,6 +22,13 @@ constexpr int kMaxDim = 256;
 __device__ __forceinline__ uint32_t sw128_offset(int blk, int rows, int row, int pos_bytes) {
   const int chunk = (pos_bytes >> 4) ^ (row & 7);
   return (uint32_t)(blk * rows * 128 + row * 128 + chunk * 16 + (pos_bytes & 15));
+}
+
+// The same for the 128-byte swizzle of 32-byte atoms (TF32 MN-major
+// operands): the 32-byte chunk index is XORed with (row & 3).
+__device__ __forceinline__ uint32_t sw128a32_offset(int blk, int rows, int row, int pos_bytes) {
+  const int chunk = (pos_bytes >> 5) ^ (row & 3);
+  return (uint32_t)(blk * rows * 128 + row * 128 + chunk * 32 + (pos_bytes & 31));
 }
 
 template <bool BF16>
@@ -50,13 +58,15 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
   // MN-major: blocks along M (or N), rows = K.
   for (int idx = tid; idx < M * K; idx += blockDim.x) {
     const int m = idx / K, k = idx % K;
-    uint32_t off = a_mn ? sw128_offset(m / W, K, k, (m % W) * E)
+    uint32_t off = a_mn ? (BF16 ? sw128_offset(m / W, K, k, (m % W) * E)
+                                : sw128a32_offset(m / W, K, k, (m % W) * E))
                         : sw128_offset(k / W, M, m, (k % W) * E);
     *reinterpret_cast<T*>(sA + off) = gA[idx];
   }
   for (int idx = tid; idx < N * K; idx += blockDim.x) {
     const int n = idx / K, k = idx % K;
-    uint32_t off = b_mn ? sw128_offset(n / W, K, k, (n % W) * E)
+    uint32_t off = b_mn ? (BF16 ? sw128_offset(n / W, K, k, (n % W) * E)
+                                : sw128a32_offset(n / W, K, k, (n % W) * E))
                         : sw128_offset(k / W, N, n, (k % W) * E);
     *reinterpret_cast<T*>(sB + off) = gB[idx];
   }
@@ -113,14 +123,17 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
     constexpr int KSTEP = 32 / E;  // elements of K per instruction (32 bytes)
     for (int ks = 0; ks < K / KSTEP; ++ks) {
       uint64_t ad = 0, bd;
+      // MN-major: a K step is KSTEP rows; LBO = bytes between MN blocks
       if (a_mn) {
-        ad = sw128_desc(a0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u);
+        ad = BF16 ? sw128_desc(a0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u)
+                  : mn32_desc(a0 + ks * KSTEP * 128, (uint32_t)K * 128u);
       } else {
         const int kb = ks * 32;
         ad = sw128_desc(a0 + (kb / 128) * M * 128 + (kb % 128), 16u, 1024u);
       }
       if (b_mn) {
-        bd = sw128_desc(b0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u);
+        bd = BF16 ? sw128_desc(b0 + ks * KSTEP * 128, (uint32_t)K * 128u, 1024u)
+                  : mn32_desc(b0 + ks * KSTEP * 128, (uint32_t)K * 128u);
       } else {
         const int kb = ks * 32;
         bd = sw128_desc(b0 + (kb / 128) * N * 128 + (kb % 128), 16u, 1024u);

@@ -316,7 +316,9 @@ attn_status attn_bwd_check_device_error(int32_t clear_it);
  * with tcgen05.mma from operands staged in 128-byte-swizzled shared memory.
  *   dtype: ATTN_F32 (TF32) or ATTN_BF16; A and B are fp32 or bf16 row-major
  *   host layouts [M][K] / [N][K]; a_mn / b_mn = 1 stage the operand in
- *   MN-major form (transposed tile) instead of K-major.
+ *   MN-major form (rows along K) instead of K-major; a TF32 MN-major operand
+ *   uses the 128-byte swizzle of 32-byte atoms, the layout the tile kernels
+ *   read Q, dO, K and V in.
  *   a_tmem = 1 takes A from tensor memory instead (row m in the lane of
  *   accumulator row m, K along 32-bit columns, two bf16 per column).
  *   M in {64, 128}, N in {32, 64, 128, 256} (N <= 256), K a multiple of the

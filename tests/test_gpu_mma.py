@@ -1,5 +1,6 @@
 """Tensor-core building block: one tcgen05.mma tile from 128-byte-swizzled
-shared memory (K-major and MN-major operands), checked against a CPU product."""
+shared memory (K-major and MN-major operands; TF32 MN-major operands in the
+128-byte swizzle of 32-byte atoms), checked against a CPU product."""
 import numpy as np
 import pytest
 
@@ -16,8 +17,6 @@ def _tf32_trunc(x):
                                  (64, 128)])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 def test_single_tile_product(dtype, M, N, a_mn, b_mn):
-    if dtype == 0 and (a_mn or b_mn):
-        pytest.skip("TF32 operands are read K-major only with the 16-byte-atom swizzle")
     W_ = 32 if dtype == 0 else 64
     if (a_mn and M % W_) or (b_mn and N % W_):
         pytest.skip("an MN-major operand spans whole 128-byte blocks")
@@ -50,8 +49,6 @@ def test_single_tile_product(dtype, M, N, a_mn, b_mn):
 @pytest.mark.parametrize("M,N", [(128, 32), (128, 64), (128, 128), (64, 32), (64, 64)])
 @pytest.mark.parametrize("b_mn", [0, 1])
 def test_a_operand_from_tmem(dtype, M, N, b_mn):
-    if dtype == 0 and b_mn:
-        pytest.skip("TF32 operands are read K-major only with the 16-byte-atom swizzle")
     W_ = 32 if dtype == 0 else 64
     if b_mn and N % W_:
         pytest.skip("an MN-major operand spans whole 128-byte blocks")
