@@ -67,6 +67,10 @@ namespace {
 
 template <bool BF16, int D>
 struct Cfg;
+// MNCOPY (fp32): GEMM3/4 read a second copy of the tile's Q / dO and GEMM5 a
+// second copy of K, fetched in the 128-byte swizzle of 32-byte atoms and
+// read MN-major; the softmax writes dS' as [query][key] for GEMM5.  Without
+// it (bf16) one copy of each tile serves both majors and dS' is [key][query].
 // INPL: P and dS' overwrite S^T and dP^T in tensor memory (no separate P /
 // dS' columns), and the shared-memory dS' tile of query tile t is written over
 // tile t's own natural Q / dO stage (GEMM1/2 are done with it by then), which
@@ -88,25 +92,25 @@ struct Cfg;
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
   static constexpr int BN = 128, BM = 64, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 3;
-  static constexpr bool KMAJ = true, DQT = true, INPL = true, VTM = true;
+  static constexpr bool MNCOPY = true, DQT = true, INPL = true, VTM = true;
   static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
   static constexpr int BN = 128, BM = 32, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 1;
-  static constexpr bool KMAJ = true, DQT = true, INPL = true, VTM = true;
+  static constexpr bool MNCOPY = true, DQT = true, INPL = true, VTM = true;
   static constexpr bool SPLITQ = true, VGL = true, DQA = true, DQRED = true, FRAG = false;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
   static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
-  static constexpr bool KMAJ = false, DQT = false, INPL = false, VTM = false;
+  static constexpr bool MNCOPY = false, DQT = false, INPL = false, VTM = false;
   static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
   static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
-  static constexpr bool KMAJ = false, DQT = true, INPL = false, VTM = false;
+  static constexpr bool MNCOPY = false, DQT = true, INPL = false, VTM = false;
   static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
 };
 
@@ -118,7 +122,7 @@ struct Layout {
   using C = Cfg<BF16, D>;
   static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB,
                        PB = C::PB;
-  static constexpr bool KMAJ = C::KMAJ, DQT = C::DQT, INPL = C::INPL, VTM = C::VTM;
+  static constexpr bool MNCOPY = C::MNCOPY, DQT = C::DQT, INPL = C::INPL, VTM = C::VTM;
   static constexpr bool SPLITQ = C::SPLITQ, VGL = C::VGL, DQA = C::DQA, DQRED = C::DQRED,
                         FRAG = C::FRAG;
   static constexpr int NDO = SPLITQ ? C::NDO : NAT;  // dO slots (= NAT unless SPLITQ)
@@ -135,7 +139,7 @@ struct Layout {
   // natural ring [NAT]: separate Q and dO rings, or (INPL) stages of
   // [Q tile][dO tile] that later hold the tile's dS' [BM rows][BN keys], or
   // (SPLITQ) NAT Q slots (later dS') and NDO dO slots
-  static constexpr int OFF_Q = OFF_KT + (KMAJ ? K_BYTES : 0);
+  static constexpr int OFF_Q = OFF_KT + (MNCOPY ? K_BYTES : 0);
   static constexpr bool JOINT = INPL && !SPLITQ;  // [Q | dO] stages
   static constexpr int NAT_STRIDE = JOINT ? 2 * Q_BYTES : Q_BYTES;
   static constexpr int OFF_DO = OFF_Q + (JOINT ? Q_BYTES : NAT * Q_BYTES);
@@ -144,9 +148,9 @@ struct Layout {
   static constexpr int OFF_DOT = OFF_QT + TR * Q_BYTES;
   // bf16: dS'^T [BN rows][BM] (GEMM4 A, GEMM5 operand); fp32: PB x dS' [BM rows][BN]
   static constexpr int OFF_DS = OFF_DOT + TR * Q_BYTES;
-  static constexpr int OFF_DSN = OFF_DS + (KMAJ ? 0 : P_BYTES);
+  static constexpr int OFF_DSN = OFF_DS + (MNCOPY ? 0 : P_BYTES);
   static constexpr int ROW_ST = 4;  // stages of the LSE2 / Delta ring
-  static constexpr int OFF_LSE = OFF_DSN + (KMAJ && !INPL ? PB * P_BYTES : 0);
+  static constexpr int OFF_LSE = OFF_DSN + (MNCOPY && !INPL ? PB * P_BYTES : 0);
   // VTM: V lands in the (not yet used) MN-major copy ring and is moved into
   // tensor memory before the first MN-major copies are fetched
   static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
@@ -169,16 +173,16 @@ struct Layout {
   static constexpr int NAT_TX = SPLITQ ? Q_BYTES : 2 * Q_BYTES;
   static constexpr int TR_TX = 2 * Q_BYTES;
   static constexpr int ROW_TX = 2 * BM * 4;
-  static constexpr int KV_TX = ((KMAJ ? 3 : 2) - (VGL ? 1 : 0)) * K_BYTES;
-  // GEMM5 shape: dQ^T [D (padded to 128 if not KMAJ), BM] or dQ [BM, D]
-  static constexpr int M5 = DQT ? (KMAJ ? D : 128) : BM;
+  static constexpr int KV_TX = ((MNCOPY ? 3 : 2) - (VGL ? 1 : 0)) * K_BYTES;
+  // GEMM5 shape: dQ^T [D (padded to 128 if not MNCOPY), BM] or dQ [BM, D]
+  static constexpr int M5 = DQT ? (MNCOPY ? D : 128) : BM;
   static constexpr int N5 = DQT ? BM : D;
   // tensor memory columns: NSB x (S^T, dP^T), PB x P^T (fp32: one column per
   // element; bf16: two per column), fp32: PB x dS'^T, then dV, dK, dQ
   static constexpr int PCOLS = BF16 ? BM / 2 : BM;
   static constexpr int T_P = 2 * BM * NSB;
   static constexpr int T_DS = T_P + (INPL ? 0 : PB * PCOLS);
-  static constexpr int T_DV = T_DS + (KMAJ && !INPL ? PB * BM : 0), T_DK = T_DV + D,
+  static constexpr int T_DV = T_DS + (MNCOPY && !INPL ? PB * BM : 0), T_DK = T_DV + D,
                        T_DQ = T_DK + D;
   static constexpr int T_V = T_DQ + (DQA ? 0 : N5);
   static constexpr int T_USED = T_V + (VTM ? D : 0);
@@ -188,18 +192,18 @@ struct Layout {
   static_assert(T_USED <= 512 && TR_TX > 0, "tensor memory budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(COLS % 16 == 0, "softmax column chunks");
-  static_assert(!KMAJ || (D % W == 0 && BM % KSTEP == 0 && TR >= 1), "MN-major copies");
-  static_assert(KMAJ || NAT >= 2, "stages are released only after GEMM3/4");
+  static_assert(!MNCOPY || (D % W == 0 && BM % KSTEP == 0 && TR >= 1), "MN-major copies");
+  static_assert(MNCOPY || NAT >= 2, "stages are released only after GEMM3/4");
   static_assert(PB == 1 || PB == 2, "P / dS buffers");
   static_assert(BN == 64 || BN == 128, "key tile");
-  static_assert(!INPL || (KMAJ && !BF16 && NAT_STRIDE >= P_BYTES && NAT >= 3),
+  static_assert(!INPL || (MNCOPY && !BF16 && NAT_STRIDE >= P_BYTES && NAT >= 3),
                 "in-place P / dS' is the fp32 layout; dS' fits a natural stage");
   static_assert(!VTM || (INPL && BN == 128 && (VGL || (2 * TR * Q_BYTES >= K_BYTES && D / W == 2))),
                 "V staging through the MN-major copy ring, one column block per softmax half");
   static_assert(!SPLITQ || (INPL && NDO >= 1), "split rings hold dS' in the Q slot");
-  static_assert(!DQA || (INPL && NSB == 2 && KMAJ && BF16 == false && L_N5_FITS(N5, BM)),
+  static_assert(!DQA || (INPL && NSB == 2 && MNCOPY && BF16 == false && L_N5_FITS(N5, BM)),
                 "dQ^T aliases the P columns of its score buffer");
-  static_assert(!DQRED || (DQT && KMAJ && M5 == 128 && N5 == BM), "register dQ reduction");
+  static_assert(!DQRED || (DQT && MNCOPY && M5 == 128 && N5 == BM), "register dQ reduction");
   static_assert(!FRAG || (INPL && BM == 64 && D == 64), "16x256b softmax fragments");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_5d(smem + L::OFF_K, &tm_k, kv_full, 0, w.k0, 0, w.kvh, w.b);
       if constexpr (!L::VGL)
         tma_load_5d(smem + L::OFF_VLOAD, &tm_v, kv_full, 0, w.k0, 0, w.kvh, w.b);
-      if constexpr (L::KMAJ)  // MN-major copy of K for GEMM5
+      if constexpr (L::MNCOPY)  // MN-major copy of K for GEMM5
         tma_load_5d(smem + L::OFF_KT, &tm_kt, kv_full, 0, w.k0, 0, w.kvh, w.b);
       int nat_issued = 0, row_issued = 0, do_issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -589,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (fp32) the tile's Q and dO again, [D / W blocks][BM rows][W columns] in
     // the 32-byte-atom swizzle, in a ring of its own so it never holds up the
     // natural tiles that GEMM1/2 wait for
-    if constexpr (L::KMAJ) {
+    if constexpr (L::MNCOPY) {
       if (elect_one_sync() && T > 0) {
         tma_prefetch_desc(&tm_qt);
         tma_prefetch_desc(&tm_dot);
@@ -622,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = make_idesc(BF16, BN, BM, false, false);
       // GEMM3/4 read dO / Q MN-major; GEMM5 reads K MN-major (and, bf16, dS')
       constexpr uint32_t id_acc = make_idesc(BF16, BN, D, false, true);
-      constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, true, !L::KMAJ);
+      constexpr uint32_t id_dq = make_idesc(BF16, L::M5, L::N5, true, !L::MNCOPY);
       // K-major tiles: LBO unused, SBO = 8 rows x 128 B
       const uint64_t dK = sw128_desc(smem_u32(smem + L::OFF_K), 16, 1024);
       const uint64_t dV = sw128_desc(smem_u32(smem + L::OFF_V), 16, 1024);
@@ -674,22 +678,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&s_full[b]);
         // natural tiles done with (INPL: the stage then holds dS' until GEMM5)
-        if constexpr (L::KMAJ && !L::INPL) mma_commit(&nat_empty[s]);
+        if constexpr (L::MNCOPY && !L::INPL) mma_commit(&nat_empty[s]);
         if constexpr (L::SPLITQ) mma_commit(&do_empty[so]);
         return true;
       };
       auto issue_back34 = [&](int t) -> bool {  // GEMM3, GEMM4 of tile t
         if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, a.err)) return false;
-        const int s = t % NAT, r = L::KMAJ ? t % TR : 0, pb = t % PB, b = t % NSB;
+        const int s = t % NAT, r = L::MNCOPY ? t % TR : 0, pb = t % PB, b = t % NSB;
         // P^T and (fp32) dS'^T: A operands of GEMM3/4 in tensor memory
         const uint32_t t_p = L::INPL ? tmem + b * 2 * BM : tmem + L::T_P + pb * L::PCOLS;
         const uint32_t t_ds = L::INPL ? t_p + BM : tmem + L::T_DS + pb * BM;
-        if constexpr (L::KMAJ) {
+        if constexpr (L::MNCOPY) {
           if (!mbar_wait(&tr_full[r], (t / TR) & 1, a.err)) return false;
         }
         tc_fence_after();
         uint64_t bdo0, bq0;
-        if constexpr (L::KMAJ) {  // MN-major copies of the tile's dO / Q
+        if constexpr (L::MNCOPY) {  // MN-major copies of the tile's dO / Q
           bdo0 = adv(aDOT0, r * L::Q_BYTES);
           bq0 = adv(aQT0, r * L::Q_BYTES);
         } else {  // natural tiles [BM rows][D] read MN-major
@@ -719,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc = (t > 0 || ks > 0) ? 1u : 0u;
           // 8 TMEM columns hold one K step (8 tf32, or 16 bf16 packed in pairs)
           mma_ts<BF16>(tmem + L::T_DV, t_p + ks * 8, adv(bdo0, ba), id_acc, acc);
-          if constexpr (L::KMAJ) {
+          if constexpr (L::MNCOPY) {
             mma_ts<BF16>(tmem + L::T_DK, t_ds + ks * 8, adv(bq0, ba), id_acc, acc);
           } else {
             mma_ss<BF16>(tmem + L::T_DK, adv(dS, pa), adv(bq0, ba), id_acc, acc);
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         }
         if constexpr (L::INPL) mma_commit(&pfree[b]);  // score buffer b reusable
-        if constexpr (L::KMAJ) mma_commit(&tr_empty[r]);  // GEMM5 does not read them
+        if constexpr (L::MNCOPY) mma_commit(&tr_empty[r]);  // GEMM5 does not read them
         return true;
       };
       auto issue_g5 = [&](int t) -> bool {  // GEMM5 of tile t
@@ -747,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_dq = L::DQA ? tmem + (uint32_t)(b * 2 * BM) : tmem + L::T_DQ;
 #pragma unroll
         for (int ks = 0; ks < BN / L::KSTEP; ++ks) {
-          if constexpr (L::KMAJ) {  // dQ^T = K^T . dS'^T: K MN-major, dS' K-major
+          if constexpr (L::MNCOPY) {  // dQ^T = K^T . dS'^T: K MN-major, dS' K-major
             const uint32_t kb = ks * 32;
             const uint32_t ka = ks * L::KSTEP * 128;
             const uint32_t na = (L::INPL ? s * L::NAT_STRIDE : pb * L::P_BYTES) +
@@ -763,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma5_done);
         mma_commit(&mma5_par[pb]);
-        if constexpr (!L::KMAJ || L::INPL) mma_commit(&nat_empty[s]);
+        if constexpr (!L::MNCOPY || L::INPL) mma_commit(&nat_empty[s]);
         return true;
       };
       // GEMM1/2 run NSB tiles ahead of GEMM3-5: front(t + NSB) only needs the
