@@ -4,8 +4,9 @@
   wait gives up after about a second, the device error word reads
   ATTN_ERR_TIMEOUT, clearing it works, and the context then runs a backward
   pass that matches the oracle.
-* Every output of the backward (default and deterministic dQ), the LSE sweep
-  and both decode passes is written into the middle of a larger buffer whose
+* Every output of the backward (default and deterministic dQ), the LSE sweep,
+  the fused forward and both decode passes is written into the middle of a
+  larger buffer whose
   guard regions hold a sentinel bit pattern; the guards must be untouched and
   the outputs must match the oracle (the parity suites' shapes: ragged tiles,
   Sq = Sk = 1, GQA with a window, mask with dropout).
@@ -147,6 +148,34 @@ def test_lse_writes_stay_inside_output(name, dtype):
     empty = ref == OA.EMPTY_ROW_LSE
     assert np.all(got[empty] == np.float32(3.0e38))
     assert np.all(np.abs(got[~empty] - ref[~empty]) <= lse_bound(p, Q, K, mask, ref)[~empty])
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("name", sorted(GUARD_CASES))
+def test_forward_writes_stay_inside_outputs(name, dtype):
+    import torch
+    import attention_backward_pass_gb300 as ab
+    p = copy.copy(GUARD_CASES[name][0])
+    p.dtype = dtype
+    Q, K, V, _, mask = W.make_inputs(p, 79)
+    tdt = torch.bfloat16 if dtype == W.DTYPE_BF16 else torch.float32
+    to = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda().to(tdt)  # noqa: E731
+    m = torch.from_numpy(mask).cuda() if mask is not None else None
+    bo, O = _guarded(p.q_shape(), tdt)
+    bl, LSE = _guarded((p.batch, p.num_heads, p.seq_q), torch.float32)
+    ws = torch.empty(ab.fwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    ab.attn_fwd(p, to(Q), to(K), to(V), m, O, LSE, ws)
+    torch.cuda.synchronize()
+    assert ab.check_device_error() == 0
+    assert _guards_intact(bo) and _guards_intact(bl)
+    f = lambda a: a.astype(np.float64)  # noqa: E731
+    O_ref, LSE_ref = OA.forward(p, f(Q), f(K), f(V), mask)
+    assert rel_err(O.float().cpu().numpy(), O_ref) <= TOL[dtype]
+    got = LSE.cpu().numpy().astype(np.float64)
+    empty = LSE_ref == OA.EMPTY_ROW_LSE
+    assert np.all(got[empty] == np.float32(3.0e38))
+    bound = lse_bound(p, Q, K, mask, LSE_ref)
+    assert np.all(np.abs(got[~empty] - LSE_ref[~empty]) <= bound[~empty])
 
 
 # shapes of the decode parity suite
