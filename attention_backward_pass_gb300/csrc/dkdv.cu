@@ -86,32 +86,33 @@ struct Cfg;
 // DQA: the dQ^T accumulator of tile t lives in the P columns of score buffer
 //   t % NSB: GEMM5 (t) is issued once GEMM3/4 (t) are complete, and GEMM1/2
 //   (t + NSB) wait until the dQ warps have drained it.
-// DQRED: the dQ warps add dQ into global memory with fp32 reductions straight
-//   from registers (no shared-memory staging tile).
+// DQSLOT: the dQ warps stage dQ of tile t in tile t's own Q slot (which held
+//   its dS' until GEMM5) and add it with one TMA reduce-add; the slot goes
+//   back to the producer once the copy engine has read it.
 // FRAG: the unmasked fp32 softmax uses 16x256b fragments (BM = 64 only).
 template <>
 struct Cfg<false, 64> {  // fp32, D = 64
   static constexpr int BN = 128, BM = 64, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 3;
   static constexpr bool MNCOPY = true, DQT = true, INPL = true, VTM = true;
-  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = true;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQSLOT = false, FRAG = true;
 };
 template <>
 struct Cfg<false, 128> {  // fp32, D = 128
   static constexpr int BN = 128, BM = 32, NAT = 3, TR = 1, NSB = 2, PB = 1, NDO = 1;
   static constexpr bool MNCOPY = true, DQT = true, INPL = true, VTM = true;
-  static constexpr bool SPLITQ = true, VGL = true, DQA = true, DQRED = true, FRAG = false;
+  static constexpr bool SPLITQ = true, VGL = true, DQA = true, DQSLOT = true, FRAG = false;
 };
 template <>
 struct Cfg<true, 64> {  // bf16, D = 64
   static constexpr int BN = 128, BM = 128, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
   static constexpr bool MNCOPY = false, DQT = false, INPL = false, VTM = false;
-  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQSLOT = false, FRAG = false;
 };
 template <>
 struct Cfg<true, 128> {  // bf16, D = 128
   static constexpr int BN = 128, BM = 64, NAT = 3, TR = 0, NSB = 1, PB = 1, NDO = 3;
   static constexpr bool MNCOPY = false, DQT = true, INPL = false, VTM = false;
-  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQRED = false, FRAG = false;
+  static constexpr bool SPLITQ = false, VGL = false, DQA = false, DQSLOT = false, FRAG = false;
 };
 
 // the dQ^T accumulator [M5 lanes][N5 columns] fits in the BM P columns
@@ -123,7 +124,7 @@ struct Layout {
   static constexpr int BM = C::BM, BN = C::BN, NAT = C::NAT, TR = C::TR, NSB = C::NSB,
                        PB = C::PB;
   static constexpr bool MNCOPY = C::MNCOPY, DQT = C::DQT, INPL = C::INPL, VTM = C::VTM;
-  static constexpr bool SPLITQ = C::SPLITQ, VGL = C::VGL, DQA = C::DQA, DQRED = C::DQRED,
+  static constexpr bool SPLITQ = C::SPLITQ, VGL = C::VGL, DQA = C::DQA, DQSLOT = C::DQSLOT,
                         FRAG = C::FRAG;
   static constexpr int NDO = SPLITQ ? C::NDO : NAT;  // dO slots (= NAT unless SPLITQ)
   static constexpr int E = BF16 ? 2 : 4;  // element bytes
@@ -155,15 +156,16 @@ struct Layout {
   // tensor memory before the first MN-major copies are fetched
   static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
-  // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per pass
-  static constexpr int STG_D = (DQT && !DQRED) ? (D > 64 ? 64 : D) : 0;
+  // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per
+  // pass (DQSLOT: all D in one pass, in the tile's Q slot, no region of its own)
+  static constexpr int STG_D = DQT ? (DQSLOT ? D : (D > 64 ? 64 : D)) : 0;
   static constexpr int OFF_STG = OFF_DELTA + ROW_ST * BM * 4;
   // (fp32, D=64) dropout keep bits of two query tiles, [2][BN keys][BM / 16]
   // x 16 bits, drawn by the dQ warps one tile ahead of the softmax warps; the
   // other configurations draw them in the softmax warps
   static constexpr bool DBITS = !BF16 && D == 64;
   static constexpr int NCH = BM / 16;
-  static constexpr int OFF_BITS = OFF_STG + BM * STG_D * 4;
+  static constexpr int OFF_BITS = OFF_STG + (DQSLOT ? 0 : BM * STG_D * 4);
   static constexpr int OFF_BAR = OFF_BITS + (DBITS ? 2 * BN * NCH * 2 : 0);
   static constexpr int NUM_BARS = 2 * NAT + 2 * TR + 2 * ROW_ST + 4 * NSB + 2 + PB + 9 +
                                   2 * NDO + 2 * NSB;
@@ -203,7 +205,9 @@ struct Layout {
   static_assert(!SPLITQ || (INPL && NDO >= 1), "split rings hold dS' in the Q slot");
   static_assert(!DQA || (INPL && NSB == 2 && MNCOPY && BF16 == false && L_N5_FITS(N5, BM)),
                 "dQ^T aliases the P columns of its score buffer");
-  static_assert(!DQRED || (DQT && MNCOPY && M5 == 128 && N5 == BM), "register dQ reduction");
+  static_assert(!DQSLOT || (SPLITQ && INPL && DQT && MNCOPY && M5 == D && N5 == BM &&
+                              BM * D * 4 == Q_BYTES),
+                "dQ [BM][D] fp32 staged in the tile's Q slot");
   static_assert(!FRAG || (INPL && BM == 64 && D == 64), "16x256b softmax fragments");
   static_assert(M5 == 64 || M5 == 128, "GEMM5 rows");
 };
@@ -767,7 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma5_done);
         mma_commit(&mma5_par[pb]);
-        if constexpr (!L::MNCOPY || L::INPL) mma_commit(&nat_empty[s]);
+        // (DQSLOT: the dQ warps release the slot after staging dQ in it)
+        if constexpr ((!L::MNCOPY || L::INPL) && !L::DQSLOT) mma_commit(&nat_empty[s]);
         return true;
       };
       // GEMM1/2 run NSB tiles ahead of GEMM3-5: front(t + NSB) only needs the
@@ -1172,8 +1177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per tile: read the GEMM5 accumulator out of TMEM, release it, and add
     // it into the fp32 dQ accumulator in global memory.  The transposed
     // accumulator (dQ^T: lanes = head dim, columns = queries) is staged through
-    // shared memory as [query][d] so the adds go out as 16-byte vector
-    // atomics along each dQ row.
+    // shared memory as [query][d] (fp32, D = 128: in the tile's own Q slot)
+    // and added by TMA reduce-adds; a row-per-lane dQ (bf16, D = 64) goes out
+    // as 16-byte vector atomics along each dQ row.
     const int quad = warp & 3;
     const int tid = threadIdx.x - 384;  // 0..127
     const int r = acc_row<L::M5>(quad * 32 + lane);  // accumulator row, or -1
@@ -1216,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = t / w.tiles_per_head;
       const int h = w.kvh * a.group + g;
       const int q0 = w.q_first + (t % w.tiles_per_head) * BM;
-      // every dQ thread is also done reading the staging tile of tile t-1
+      // (staged dQ) every dQ thread is also done writing tile t - 1's stage
       if (!dq_group_all(mbar_wait(mma5_done, t & 1, a.err))) break;
       if (t == 0 && a.pdl) griddep_wait();  // the accumulator is zeroed by the prepare kernel
       tc_fence_after();
@@ -1240,23 +1246,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kt = w.k0 / BN;
       float* gbase = a.det ? a.dq_acc + row_offset(0, kt * a.B + w.b, h, q0, a.H, a.Sq, D)
                            : a.dq_acc + row_offset(a.layout, w.b, h, q0, a.H, a.Sq, D);
-      if constexpr (L::DQRED) {
-        // lane r holds head-dim column r of dQ^T for the tile's BM queries:
-        // fp32 reductions (deterministic mode: stores into this key tile's
-        // slice), coalesced along d across the warp
-        if (r >= 0) {
-          const long long qstride = a.det ? D : rstride;
-          float* dst = gbase + r;
+      if constexpr (L::DQSLOT) {
+        // stage [BM queries][D] fp32 in the tile's Q slot (GEMM5, the last
+        // reader of its dS', is complete: mma5_done), then one TMA
+        // reduce-add (deterministic mode: a store into this key tile's
+        // slice); rows past Sq fall outside the tensor map and are skipped
+        const int s = t % NAT;
+        float* slot = reinterpret_cast<float*>(smem + L::OFF_Q + s * L::NAT_STRIDE);
 #pragma unroll
-          for (int c = 0; c < BM; ++c) {  // v[] stays in registers: constant indices
-            if (c < nq) {
-              if (a.det)
-                dst[c * qstride] = v[c];
-              else
-                atomicAdd(dst + c * qstride, v[c]);
-            }
-          }
+        for (int c = 0; c < BM; ++c) slot[c * D + r] = v[c];
+        fence_proxy_async_smem();
+        dq_group_sync();
+        if (tid == 0) {
+          if (a.det)
+            tma_store_4d(&tm_dq, slot, 0, q0, h, kt * a.B + w.b);
+          else
+            tma_reduce_add_4d(&tm_dq, slot, 0, q0, h, w.b);
+          bulk_commit();
+          bulk_wait_read();  // the copy engine has read the slot: back to the producer
+          mbar_arrive(&nat_empty[s]);
         }
+        (void)gbase;
+        (void)nq;
       } else if constexpr (L::DQT) {
         // stage [BM queries][STG d] and hand the tile to the TMA engine as one
         // reduce-add (rows past Sq fall outside the tensor map and are skipped)
