@@ -404,6 +404,10 @@ attn_status tiles_impl(const attn_bwd_params* p, const void* Q, const void* K, c
                bn) != CUDA_SUCCESS ||
       make_map(&maps.v, V, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch, p->layout,
                bn) != CUDA_SUCCESS ||
+      make_map(&maps.dk, dK, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch,
+               p->layout, bn) != CUDA_SUCCESS ||
+      make_map(&maps.dv, dV, p->dtype, p->head_dim, p->seq_k, p->num_kv_heads, p->batch,
+               p->layout, bn) != CUDA_SUCCESS ||
       (p->deterministic
            ? make_map_dq(&maps.dq, pl.dqp, p->head_dim, p->seq_q, p->num_heads,
                          p->batch * ((p->seq_k + bn - 1) / bn), ATTN_LAYOUT_BHSD,

@@ -49,7 +49,8 @@
 //   warps 4-11   softmax: warp w serves TMEM sub-partition w % 4 (its key
 //                rows) and half (w - 4) / 4 of the query columns; turns S^T
 //                and dP^T into P o M and dS', stores them as MMA operands, and
-//                at the end writes dK and dV
+//                at the end stages dK and dV in shared memory for two TMA
+//                stores
 //   warps 12-15  dQ: drain the GEMM5 accumulator into global memory
 // Accumulators with M = 64 rows live in lanes 0-15 of each 32-lane TMEM
 // sub-partition (row r -> lane (r / 16) * 32 + r % 16); M = 128 rows map
@@ -155,6 +156,10 @@ struct Layout {
   // VTM: V lands in the (not yet used) MN-major copy ring and is moved into
   // tensor memory before the first MN-major copies are fetched
   static constexpr int OFF_VLOAD = VTM ? OFF_QT : OFF_V;
+  // dK / dV staged for their TMA stores once every product is complete: dK
+  // over the K tile, dV over K's MN-major copy (fp32) or the V tile (bf16)
+  static constexpr int OFF_DKST = OFF_K;
+  static constexpr int OFF_DVST = MNCOPY ? OFF_KT : OFF_V;
   static constexpr int OFF_DELTA = OFF_LSE + ROW_ST * BM * 4;
   // dQ staging tile [BM][STG_D] fp32 (query-major), STG_D head-dim columns per
   // pass (DQSLOT: all D in one pass, in the tile's Q slot, no region of its own)
@@ -318,6 +323,20 @@ __device__ __forceinline__ void dq_group_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Named barrier 2 over the 256 softmax threads with the same vote.
+__device__ __forceinline__ bool softmax_group_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
 
 struct TileWork {
   int b, kvh, k0, q_begin, q_end, q_first, tiles_per_head, total;
@@ -449,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_qt,
                 const __grid_constant__ CUtensorMap tm_kt,
                 const __grid_constant__ CUtensorMap tm_dot,
-                const __grid_constant__ CUtensorMap tm_dq, const TileArgs a) {
+                const __grid_constant__ CUtensorMap tm_dq,
+                const __grid_constant__ CUtensorMap tm_dk,
+                const __grid_constant__ CUtensorMap tm_dv, const TileArgs a) {
   using L = Layout<BF16, D>;
   constexpr int BM = L::BM, NAT = L::NAT, TR = L::TR, NSB = L::NSB, PB = L::PB, BN = L::BN,
                 W = L::W, E = L::E;
@@ -1124,18 +1145,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&row_empty[rs]);
     }
     // --------------------------------------------------------- dK / dV epilogue
+    // Each lane's key row of dK and dV goes into shared memory (regions idle
+    // once every product is complete) in the 128-byte swizzle of the key-tile
+    // maps, and one thread stores both tiles with two TMA copies; rows past
+    // the end of the sequence fall outside the maps and are not written.
+    // Every softmax thread reaches the vote, so the group cannot split.
     bool have = ok && T > 0;
     if (have) {
       have = warp_wait(acc_done, 0, a.err);
       tc_fence_after();
     }
-    if (have || T == 0) {
-      const long long off = row_offset(a.layout, w.b, w.kvh, key_ok ? kj : 0, a.Hkv, a.Sk, D);
+    const bool stage = have || T == 0;
+    if (stage) {
+      uint8_t* sdk = smem + L::OFF_DKST;
+      uint8_t* sdv = smem + L::OFF_DVST;
       constexpr int DH = D / 2;  // this warp's half of the head dimension
 #pragma unroll 1
       for (int c0 = half * DH; c0 < (half + 1) * DH; c0 += 16) {
         uint32_t rv[16], rk[16];
-        __syncwarp();  // the stores below diverge on key_ok; tcgen05.ld is warp-collective
+        __syncwarp();  // tcgen05.ld is warp-collective
         if (have) {
           tmem_ld16(tmem + lane_base + L::T_DV + c0, rv);
           tmem_ld16(tmem + lane_base + L::T_DK + c0, rk);
@@ -1144,33 +1172,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) rv[c] = rk[c] = 0u;
         }
-        if (!key_ok) {
-          // key past the end of the sequence: nothing to store
-        } else if constexpr (BF16) {
-          uint4* dv = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dV) + off + c0);
-          uint4* dk = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dK) + off + c0);
+        if (j >= 0) {
+          const int blk = c0 / W;
+          const int pos = (c0 % W) * E;
+          if constexpr (BF16) {
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = h2 * 8;
-            dv[h2] = make_uint4(pack_bf16(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1])),
-                                pack_bf16(__uint_as_float(rv[c + 2]), __uint_as_float(rv[c + 3])),
-                                pack_bf16(__uint_as_float(rv[c + 4]), __uint_as_float(rv[c + 5])),
-                                pack_bf16(__uint_as_float(rv[c + 6]), __uint_as_float(rv[c + 7])));
-            dk[h2] = make_uint4(pack_bf16(__uint_as_float(rk[c]), __uint_as_float(rk[c + 1])),
-                                pack_bf16(__uint_as_float(rk[c + 2]), __uint_as_float(rk[c + 3])),
-                                pack_bf16(__uint_as_float(rk[c + 4]), __uint_as_float(rk[c + 5])),
-                                pack_bf16(__uint_as_float(rk[c + 6]), __uint_as_float(rk[c + 7])));
-          }
-        } else {
-          uint4* dv = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.dV) + off + c0);
-          uint4* dk = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.dK) + off + c0);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int c = h2 * 8;
+              const uint32_t off = sw_off(blk, BN, j, pos + h2 * 16);
+              st_shared_v4(smem_u32(sdv + off),
+                           pack_bf16(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1])),
+                           pack_bf16(__uint_as_float(rv[c + 2]), __uint_as_float(rv[c + 3])),
+                           pack_bf16(__uint_as_float(rv[c + 4]), __uint_as_float(rv[c + 5])),
+                           pack_bf16(__uint_as_float(rv[c + 6]), __uint_as_float(rv[c + 7])));
+              st_shared_v4(smem_u32(sdk + off),
+                           pack_bf16(__uint_as_float(rk[c]), __uint_as_float(rk[c + 1])),
+                           pack_bf16(__uint_as_float(rk[c + 2]), __uint_as_float(rk[c + 3])),
+                           pack_bf16(__uint_as_float(rk[c + 4]), __uint_as_float(rk[c + 5])),
+                           pack_bf16(__uint_as_float(rk[c + 6]), __uint_as_float(rk[c + 7])));
+            }
+          } else {
 #pragma unroll
-          for (int h4 = 0; h4 < 4; ++h4) {
-            dv[h4] = make_uint4(rv[h4 * 4], rv[h4 * 4 + 1], rv[h4 * 4 + 2], rv[h4 * 4 + 3]);
-            dk[h4] = make_uint4(rk[h4 * 4], rk[h4 * 4 + 1], rk[h4 * 4 + 2], rk[h4 * 4 + 3]);
+            for (int h4 = 0; h4 < 4; ++h4) {
+              const uint32_t off = sw_off(blk, BN, j, pos + h4 * 16);
+              st_shared_v4(smem_u32(sdv + off), rv[h4 * 4], rv[h4 * 4 + 1], rv[h4 * 4 + 2],
+                           rv[h4 * 4 + 3]);
+              st_shared_v4(smem_u32(sdk + off), rk[h4 * 4], rk[h4 * 4 + 1], rk[h4 * 4 + 2],
+                           rk[h4 * 4 + 3]);
+            }
           }
         }
       }
+      fence_proxy_async_smem();
+    }
+    if (softmax_group_all(stage) && threadIdx.x == 128) {
+      tma_store_5d(&tm_dk, smem + L::OFF_DKST, 0, w.k0, 0, w.kvh, w.b);
+      tma_store_5d(&tm_dv, smem + L::OFF_DVST, 0, w.k0, 0, w.kvh, w.b);
+      bulk_commit();
+      bulk_wait_all();  // both stores complete before the CTA can exit
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ warps
@@ -1333,7 +1372,7 @@ cudaError_t launch_impl(const TileMaps& m, const TileArgs& a0, cudaStream_t stre
   const int grid = a.n_kv_tiles * a.B * a.Hkv;
   if (!pdl) {
     kern<<<grid, kThreads, L::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot,
-                                                    m.dq, a);
+                                                    m.dq, m.dk, m.dv, a);
     return cudaGetLastError();
   }
   // may start while the prepare kernel finishes: key tiles, query tiles and
@@ -1349,7 +1388,8 @@ cudaError_t launch_impl(const TileMaps& m, const TileArgs& a0, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, m.dq, a);
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, m.qt, m.kt, m.dot, m.dq, m.dk, m.dv,
+                         a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

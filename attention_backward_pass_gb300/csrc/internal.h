@@ -98,6 +98,7 @@ struct TileMaps {
   CUtensorMap q, k, v, dout;  // natural [.., S, .., D] tensors
   CUtensorMap qt, kt, dot;    // fp32: Q, K, dO again, 32-byte-atom swizzle (MN-major reads)
   CUtensorMap dq;             // fp32 dQ accumulator (reduce-add target)
+  CUtensorMap dk, dv;         // outputs, the key tiles' layout (TMA stores)
 };
 // after_prepare: programmatic dependent launch behind the prepare kernel
 cudaError_t launch_dkdv(const attn_bwd_params& p, const TileMaps& maps, const TileArgs& a,

@@ -171,6 +171,17 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* s
       : "memory");
 }
 
+// 5-D tiled store shared -> global through TMA (bulk group); elements outside
+// the tensor are not written.
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // 4-D tiled reduce-add shared -> global through TMA (bulk group), and its
 // completion controls.  The shared source must keep its contents until
 // bulk_wait_read() returns.
