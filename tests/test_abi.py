@@ -93,6 +93,25 @@ def test_null_pointers_and_mask_mismatch(lib):
     assert lib.attn_bwd(ctypes.byref(prm), *args, ctypes.c_void_p(4096 + 16), 1 << 30, None) == -5
 
 
+@pytest.mark.parametrize("which", ["dQ", "dK", "dV"])
+def test_misaligned_or_null_outputs_rejected(lib, which):
+    """dQ, dK and dV are written with 16-byte vector and TMA stores: a
+    misaligned or null output pointer is refused before anything is enqueued,
+    by attn_bwd and by the tile stage alone."""
+    prm = ab.make_params(P())
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    for bad in (ctypes.c_void_p(4096 + 4), None):
+        outs = {"dQ": fake, "dK": fake, "dV": fake}
+        outs[which] = bad
+        # attn_bwd: Q, K, V, O, dO, LSE, mask, dQ, dK, dV
+        assert lib.attn_bwd(ctypes.byref(prm), fake, fake, fake, fake, fake, fake, None,
+                            outs["dQ"], outs["dK"], outs["dV"], ws, 1 << 30, None) == -1
+        # attn_bwd_tiles: Q, K, V, dO, mask, dQ, dK, dV
+        assert lib.attn_bwd_tiles(ctypes.byref(prm), fake, fake, fake, fake, None,
+                                  outs["dQ"], outs["dK"], outs["dV"], ws, 1 << 30, None) == -1
+
+
 def test_forward_validation(lib):
     prm = ab.make_params(P())
     fake = ctypes.c_void_p(4096)
